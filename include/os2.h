@@ -1,0 +1,155 @@
+/*
+ * os2.h -- C ABI of libos2: Ozaki Scheme II emulation of an FP64 matrix
+ * product C = A * B on one NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one described in two web pages:
+ *   [Q] Qiita, "8ビットの整数で53ビットの倍精度を組み立てる。中国剰余定理をGPUに載せた
+ *       Ozaki Scheme II" (sections "行列積への当てはめ方" (the five steps),
+ *       "2の累乗による整数化(手順1と5)", "256以下の法の選び方(手順2)",
+ *       "誤差のないINT8行列積(手順3)", "高い精度での復元(手順4)").
+ *   [G] gist.science, "Improved Scaling for Fast Mode of Ozaki Scheme II"
+ *       (section "Methodik": the revised, scale-invariant fast-mode scaling).
+ *
+ * Steps: (1) per-row / per-column power-of-two scaling mu_i = 2^e_i,
+ * nu_j = 2^f_j; (2) truncation to integers A' = trunc(mu A), B' = trunc(B nu)
+ * and reduction to symmetric residues modulo N pairwise-coprime moduli
+ * p_l <= 256; (3) N exact residue matrix products, each reduced mod p_l;
+ * (4) Chinese-remainder reconstruction of the integer product X = A'B' in
+ * [-P/2, P/2), P = prod p_l; (5) C_ij = RN(X_ij * 2^-(e_i + f_j)).
+ *
+ * Conventions shared by every entry point
+ *  - All matrix pointers are DEVICE pointers owned by the caller (except in
+ *    os2_gemm_host, whose matrices live in host memory).  The library never
+ *    allocates or frees device memory.
+ *  - A is m x k ROW-major with leading dimension lda >= k (A[i*lda + h]).
+ *    B is k x n COLUMN-major with leading dimension ldb >= k
+ *    (B[j*ldb + h] = b_hj): both operands are contiguous along k.
+ *    C is m x n ROW-major with ldc >= n (C[i*ldc + j]).
+ *  - num_moduli N is in [1, 20]; the moduli are the first N of
+ *    256,255,253,251,247,241,239,233,229,227,223,217,211,199,197,193,191,181,179,173
+ *    ([Q] "256以下の法の選び方(手順2)", footnote 6).  14-16 give about
+ *    native-FP64 accuracy ([Q] "行列積の回数と性能").
+ *  - 0 <= k < 131072 (2^17): the bound that keeps residue products exact in
+ *    INT32 ([Q] "誤差のないINT8行列積(手順3)").
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every device-side entry point only enqueues work on it and
+ *    returns; argument errors are returned synchronously before anything is
+ *    enqueued.  Errors found on the device (non-finite input, a wait that
+ *    timed out) are recorded in a per-device status word that
+ *    os2_get_status() reads.  After any error the outputs are unspecified.
+ *  - Not re-entrant on one workspace: two calls in flight at the same time
+ *    must not share a workspace.
+ */
+#ifndef OS2_H
+#define OS2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OS2_OK = 0,
+  OS2_ERR_INVALID_ARG = 1,  /* bad size, leading dimension, pointer, mode or N */
+  OS2_ERR_UNSUPPORTED = 2,  /* valid but not supported (k >= 2^17, no GPU support) */
+  OS2_ERR_WORKSPACE = 3,    /* workspace missing or smaller than os2_workspace_size */
+  OS2_ERR_NONFINITE = 4,    /* an input entry is Inf or NaN (device-detected) */
+  OS2_ERR_RANGE = 5,        /* reserved: CRT bound violated (debug checks) */
+  OS2_ERR_TIMEOUT = 6,      /* a device-side wait gave up (device-detected) */
+  OS2_ERR_CUDA = 7          /* a CUDA runtime/driver call failed */
+} os2_status;
+
+typedef enum {
+  OS2_MODE_FAST = 0,      /* revised scale-invariant fast mode ([G] "Methodik") */
+  OS2_MODE_ACCURATE = 1   /* bound from one extra exact matrix product ([Q] 手順1) */
+} os2_mode;
+
+typedef enum {
+  OS2_GEMM_TC = 0,        /* tcgen05 tensor-core kernel (default) */
+  OS2_GEMM_SIMT = 1       /* plain CUDA-core int32 kernel (exact reference, slow) */
+} os2_gemm_variant;
+
+typedef enum {
+  OS2_OUT_MODP_INT8 = 0,  /* c_l = G_l mod p_l, symmetric, int8 [N][m][ldo] */
+  OS2_OUT_RAW_INT32 = 1   /* G_l itself, int32 [N][m][ldo] */
+} os2_out_kind;
+
+/* Bytes of device workspace os2_gemm needs for these sizes (0 on bad args).
+ * The workspace holds the exponents, the N FP16 residue planes of A and B
+ * (N*(m+n)*ceil64(k)*2 bytes) and the N int8 product residues
+ * (N*m*ceil16(n) bytes).  Must be 256-byte aligned. */
+size_t os2_workspace_size(int m, int n, int k, int num_moduli, int mode);
+
+/* The whole five-step emulated DGEMM, C = A*B.  Layouts above.  Returns after
+ * enqueueing on `stream`. */
+os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                    double *C, int ldc, int num_moduli, int mode, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/* Device workspace for os2_gemm_host: os2_workspace_size plus device copies
+ * of A (m*k), B (k*n) and C (m*n) doubles. */
+size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode);
+
+/* End-to-end variant of os2_gemm whose A, B, C are HOST pointers (pinned
+ * memory gives asynchronous copies).  Enqueues the host-to-device copies of A
+ * and B, the five steps, and the device-to-host copy of C on `stream`; the
+ * caller synchronises the stream before reading C. */
+os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                         double *C, int ldc, int num_moduli, int mode, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* Step 1 alone: exponents e (m int32) and f (n int32) such that
+ * mu_i = 2^e_i, nu_j = 2^f_j.  FAST: the revised formula of [G] "Methodik"
+ * with an exact integer upper bound of sum_h a_ih^2 (no workspace needed:
+ * pass NULL/0).  ACCURATE: needs os2_workspace_size(m,n,k,1,ACCURATE)
+ * bytes. */
+os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                     int num_moduli, int mode, int32_t *e, int32_t *f, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/* Step 2 alone for one operand: rows x k matrix X (row-major, ldx >= k; pass B
+ * as its n columns), exponents exps (rows int32).  Writes N planes of FP16
+ * symmetric residues, planes[(l*rows + r)*ldp + h] = sym(trunc(x_rh 2^exps_r) mod p_l),
+ * for h < ldp; entries h >= k are written as 0.  ldp >= k, ldp % 64 == 0. */
+os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t *exps,
+                        int num_moduli, void *planes, int ldp, void *stream);
+
+/* Step 3 alone: N residue matrix products from FP16 planes RA (N x m x ldp)
+ * and RB (N x n x ldp), ldp % 64 == 0, k <= ldp.  out_kind selects int8
+ * c_l = sym(G_l mod p_l) or raw int32 G_l; out is [N][m][ldo] with ldo >= n
+ * (ldo % 16 == 0 for int8, % 4 for int32).  variant: OS2_GEMM_TC or SIMT.
+ * Raw int32 output with the TC variant runs the exact-accumulation kernel. */
+os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB, int ldp,
+                             int num_moduli, int out_kind, void *out, int ldo, int variant,
+                             void *stream);
+
+/* Steps 4 and 5: from c (int8 [N][m][ldcres]) and the exponents, writes
+ * C[i*ldc + j] = RN(X_ij * 2^-(e_i + f_j)) with X the CRT value in
+ * [-P/2, P/2).  If X_out is not NULL it also receives X as 8 little-endian
+ * 32-bit limbs (two's complement) per entry, X_out[(i*n + j)*8 + u]. */
+os2_status os2_crt(int m, int n, const int8_t *c, int ldcres, int num_moduli, const int32_t *e,
+                   const int32_t *f, double *C, int ldc, uint32_t *X_out, void *stream);
+
+/* Host: the first num_moduli moduli into out; returns the count (0 on bad N). */
+int os2_moduli(int num_moduli, int32_t *out);
+
+/* Synchronises `stream`, returns the device status word of the current
+ * device and clears it. */
+os2_status os2_get_status(void *stream);
+
+/* Selects the step-3 kernel used by os2_gemm (process-wide; default TC). */
+os2_status os2_set_gemm_variant(int variant);
+
+/* Static description of a status code. */
+const char *os2_status_string(int status);
+
+/* Number of kernels os2_gemm launches for these arguments (for launch
+ * accounting); 0 on bad args. */
+int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OS2_H */

@@ -1,0 +1,259 @@
+"""Thin Python binding of libos2 (include/os2.h).
+
+Argument marshalling only: every step of the emulated GEMM runs in the CUDA
+kernels of libos2.  PyTorch provides device memory and streams.  There is no
+CPU fallback: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as ct
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, 1, 2, 3
+ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA = 4, 5, 6, 7
+MODE_FAST, MODE_ACCURATE = 0, 1
+GEMM_TC, GEMM_SIMT = 0, 1
+OUT_MODP_INT8, OUT_RAW_INT32 = 0, 1
+KP_ALIGN, CRES_ALIGN = 64, 16
+
+# every function declared in include/os2.h
+EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gemm_host",
+           "os2_scale", "os2_residues", "os2_gemm_residues", "os2_crt", "os2_moduli",
+           "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
+           "os2_gemm_launch_count")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Os2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libos2.so (building it first if it is missing and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"libos2 not built: {path} is missing")
+            _build.build()
+        L = ct.CDLL(path)
+        i, sz, vp, d = ct.c_int, ct.c_size_t, ct.c_void_p, ct.c_void_p
+        L.os2_workspace_size.argtypes = [i, i, i, i, i]
+        L.os2_workspace_size.restype = sz
+        L.os2_host_workspace_size.argtypes = [i, i, i, i, i]
+        L.os2_host_workspace_size.restype = sz
+        L.os2_gemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
+        L.os2_gemm.restype = i
+        L.os2_gemm_host.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
+        L.os2_gemm_host.restype = i
+        L.os2_scale.argtypes = [i, i, i, d, i, d, i, i, i, vp, vp, vp, sz, vp]
+        L.os2_scale.restype = i
+        L.os2_residues.argtypes = [i, i, d, i, vp, i, vp, i, vp]
+        L.os2_residues.restype = i
+        L.os2_gemm_residues.argtypes = [i, i, i, vp, vp, i, i, i, vp, i, i, vp]
+        L.os2_gemm_residues.restype = i
+        L.os2_crt.argtypes = [i, i, vp, i, i, vp, vp, d, i, vp, vp]
+        L.os2_crt.restype = i
+        L.os2_moduli.argtypes = [i, vp]
+        L.os2_moduli.restype = i
+        L.os2_get_status.argtypes = [vp]
+        L.os2_get_status.restype = i
+        L.os2_set_gemm_variant.argtypes = [i]
+        L.os2_set_gemm_variant.restype = i
+        L.os2_status_string.argtypes = [i]
+        L.os2_status_string.restype = ct.c_char_p
+        L.os2_gemm_launch_count.argtypes = [i, i, i, i, i]
+        L.os2_gemm_launch_count.restype = i
+        _lib = L
+        return L
+
+
+def status_string(st: int) -> str:
+    return load().os2_status_string(int(st)).decode()
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise Os2Error(st, where)
+
+
+def _mode(mode) -> int:
+    if isinstance(mode, str):
+        return {"fast": MODE_FAST, "accurate": MODE_ACCURATE}[mode]
+    return int(mode)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _kmat(X, name):
+    """float64 CUDA matrix whose rows are contiguous; returns (X, ld)."""
+    if not (X.is_cuda and X.dtype == torch.float64 and X.dim() == 2 and X.stride(1) == 1):
+        raise ValueError(f"{name} must be a 2-D float64 CUDA tensor with contiguous rows")
+    return X, max(X.stride(0), max(X.shape[1], 1))
+
+
+def moduli(num_moduli: int) -> list[int]:
+    out = (ct.c_int32 * 20)()
+    n = load().os2_moduli(num_moduli, out)
+    if n != num_moduli:
+        raise Os2Error(ERR_INVALID_ARG, "os2_moduli")
+    return list(out[:n])
+
+
+def workspace_size(m, n, k, num_moduli, mode="fast") -> int:
+    return int(load().os2_workspace_size(m, n, k, num_moduli, _mode(mode)))
+
+
+def host_workspace_size(m, n, k, num_moduli, mode="fast") -> int:
+    return int(load().os2_host_workspace_size(m, n, k, num_moduli, _mode(mode)))
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Caller-owned device workspace (torch allocation, 256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def launch_count(m, n, k, num_moduli, mode="fast") -> int:
+    return int(load().os2_gemm_launch_count(m, n, k, num_moduli, _mode(mode)))
+
+
+def set_gemm_variant(variant: int):
+    _check(load().os2_set_gemm_variant(int(variant)), "os2_set_gemm_variant")
+
+
+def get_status(stream=None) -> int:
+    return int(load().os2_get_status(_stream(stream)))
+
+
+def gemm(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 14, mode="fast", out=None,
+         workspace=None, stream=None) -> torch.Tensor:
+    """C = A @ Bt.T emulated with Ozaki Scheme II.
+
+    A: m x k, Bt: n x k (B = Bt.T in column-major form), float64 CUDA tensors
+    with contiguous rows.  Returns C (m x n, float64)."""
+    A, lda = _kmat(A, "A")
+    Bt, ldb = _kmat(Bt, "Bt")
+    m, k = A.shape
+    n = Bt.shape[0]
+    if Bt.shape[1] != k:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float64, device=A.device)
+    ldc = max(out.stride(0), max(n, 1))
+    need = workspace_size(m, n, k, num_moduli, mode)
+    if workspace is None:
+        workspace = alloc_workspace(need, A.device)
+    st = load().os2_gemm(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, _ptr(out), ldc, num_moduli,
+                         _mode(mode), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "os2_gemm")
+    return out
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, num_moduli: int = 14, mode="fast") -> torch.Tensor:
+    """Convenience: C = A @ B for a row-major k x n B (copied to column-major)."""
+    return gemm(A.contiguous(), B.t().contiguous(), num_moduli, mode)
+
+
+def gemm_host(A, Bt, C, num_moduli=14, mode="fast", workspace=None, stream=None):
+    """End-to-end call on HOST tensors (pinned for asynchronous copies): copies
+    in, five steps, copy out, all enqueued on `stream`; synchronise before use."""
+    for X, nm in ((A, "A"), (Bt, "Bt"), (C, "C")):
+        if X.is_cuda or X.dtype != torch.float64 or X.dim() != 2 or X.stride(1) != 1:
+            raise ValueError(f"{nm} must be a 2-D float64 host tensor with contiguous rows")
+    m, k = A.shape
+    n = Bt.shape[0]
+    need = host_workspace_size(m, n, k, num_moduli, mode)
+    if workspace is None:
+        workspace = alloc_workspace(need)
+    st = load().os2_gemm_host(m, n, k, _ptr(A), max(A.stride(0), max(k, 1)), _ptr(Bt),
+                              max(Bt.stride(0), max(k, 1)), _ptr(C), max(C.stride(0), max(n, 1)),
+                              num_moduli, _mode(mode), _ptr(workspace), workspace.numel(),
+                              _stream(stream))
+    _check(st, "os2_gemm_host")
+    return C
+
+
+def scale(A, Bt, num_moduli=14, mode="fast", stream=None):
+    """Step 1: exponents (e for rows of A, f for columns of B), int32 tensors."""
+    A, lda = _kmat(A, "A")
+    Bt, ldb = _kmat(Bt, "Bt")
+    m, k = A.shape
+    n = Bt.shape[0]
+    e = torch.empty(m, dtype=torch.int32, device=A.device)
+    f = torch.empty(n, dtype=torch.int32, device=A.device)
+    ws = None
+    nbytes = 0
+    if _mode(mode) == MODE_ACCURATE:
+        nbytes = workspace_size(m, n, k, 1, mode)
+        ws = alloc_workspace(nbytes, A.device)
+    st = load().os2_scale(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, num_moduli, _mode(mode),
+                          _ptr(e), _ptr(f), _ptr(ws), nbytes, _stream(stream))
+    _check(st, "os2_scale")
+    return e, f
+
+
+def residues(X, exps, num_moduli, ldp=None, stream=None) -> torch.Tensor:
+    """Step 2: FP16 residue planes [N, rows, ldp] of trunc(X * 2^exps)."""
+    X, ldx = _kmat(X, "X")
+    rows, k = X.shape
+    if ldp is None:
+        ldp = (max(k, 1) + KP_ALIGN - 1) // KP_ALIGN * KP_ALIGN
+    planes = torch.empty((num_moduli, rows, ldp), dtype=torch.float16, device=X.device)
+    exps = exps.to(torch.int32).contiguous()
+    st = load().os2_residues(rows, k, _ptr(X), ldx, _ptr(exps), num_moduli, _ptr(planes), ldp,
+                             _stream(stream))
+    _check(st, "os2_residues")
+    return planes
+
+
+def gemm_residues(RA, RB, k, out_kind=OUT_MODP_INT8, variant=GEMM_TC, stream=None):
+    """Step 3: N residue products of FP16 planes RA [N,m,ldp], RB [N,n,ldp].
+    Returns int8 [N, m, ldo] (mod p, symmetric) or int32 [N, m, ldo] (raw)."""
+    N, m, ldp = RA.shape
+    n = RB.shape[1]
+    if out_kind == OUT_MODP_INT8:
+        ldo = (max(n, 1) + CRES_ALIGN - 1) // CRES_ALIGN * CRES_ALIGN
+        out = torch.empty((N, m, ldo), dtype=torch.int8, device=RA.device)
+    else:
+        ldo = (max(n, 1) + 3) // 4 * 4
+        out = torch.empty((N, m, ldo), dtype=torch.int32, device=RA.device)
+    st = load().os2_gemm_residues(m, n, k, _ptr(RA), _ptr(RB), ldp, N, out_kind, _ptr(out), ldo,
+                                  variant, _stream(stream))
+    _check(st, "os2_gemm_residues")
+    return out
+
+
+def crt(cres, n, e, f, want_X=False, stream=None):
+    """Steps 4-5 from int8 residues [N, m, ldcres]; returns C (and X limbs)."""
+    N, m, ldcres = cres.shape
+    C = torch.empty((m, n), dtype=torch.float64, device=cres.device)
+    X = torch.empty((m, n, 8), dtype=torch.int32, device=cres.device) if want_X else None
+    st = load().os2_crt(m, n, _ptr(cres), ldcres, N, _ptr(e.to(torch.int32).contiguous()),
+                        _ptr(f.to(torch.int32).contiguous()), _ptr(C), max(n, 1), _ptr(X),
+                        _stream(stream))
+    _check(st, "os2_crt")
+    return (C, X) if want_X else C

@@ -1,0 +1,467 @@
+// Step 3: N exact residue matrix products on the 5th-generation tensor cores.
+//
+// [Q] "誤差のないINT8行列積(手順3)": per modulus, one integer product of the
+// residue matrices, exact in INT32 because |r_a r_b| <= 128*128 = 2^14 and the
+// inner dimension stays below 2^17.  sm_103a has no integer tcgen05 MMA, so
+// the residues are held as FP16 (exact for integers up to 2048) and multiplied
+// with tcgen05.mma kind::f16 into FP32 accumulators in tensor memory.  An FP32
+// accumulator is exact while every partial sum is an integer below 2^24 in
+// magnitude, so the k loop is cut into chunks and the accumulator is reduced
+// between chunks ("lazy" reduction: only when it could otherwise overflow):
+//
+//  KIND 0 (mod-p output): 128x256 tiles.  After each chunk of 15 k-blocks
+//    (960 terms, |partial| <= 134 + 960 * 2^14 < 2^24) the epilogue warps read
+//    the accumulator, subtract the nearest multiple of p_l and write the small
+//    remainder back; the next chunk accumulates on top of it.  Two jobs (tile x
+//    modulus) are interleaved chunk by chunk, one per TMEM buffer, so the MMA
+//    of one job runs while the other job's accumulator is being reduced.  The
+//    final reduction is the canonical symmetric residue c_l, stored as int8.
+//
+//  KIND 1 (exact int32): 128x128 tiles.  Each chunk starts a fresh FP32
+//    accumulator (ping-pong between two TMEM buffers); the epilogue converts it
+//    to int32 and adds it to a running sum held in registers.  Outputs: the raw
+//    int32 product (parity checks) and/or its row and column maxima (the bound
+//    product of the accurate mode).
+//
+// Warp roles (192 threads, one CTA per SM, persistent over jobs):
+//   warp 0     TMA producer: 128-byte-swizzled k-blocks of A and B into a
+//              multi-stage shared-memory ring (mbarrier full/empty pairs).
+//   warp 1     TMEM allocation; one elected thread issues tcgen05.mma and
+//              tcgen05.commit.
+//   warps 2-5  epilogue: tcgen05.ld / st on their 32-lane TMEM quarter.
+// Every wait is bounded; on expiry the CTA records OS2_ERR_TIMEOUT, lets its
+// copies and MMAs drain (again bounded), frees its TMEM and returns.
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "os2_internal.cuh"
+#include "ptx.cuh"
+
+using namespace os2ptx;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;               // FP16 elements per k-block (128 bytes)
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (about 2 s)
+
+template <int KIND>
+struct Cfg;
+template <>
+struct Cfg<0> {
+  static constexpr int BN = 256, STAGES = 4, TMEM_COLS = 512;
+};
+template <>
+struct Cfg<1> {
+  static constexpr int BN = 128, STAGES = 6, TMEM_COLS = 256;
+};
+
+struct Sched {
+  int m, n, kb_total;
+  int tiles_m, tiles_n, tiles;
+  int njobs;
+  int chunk, nchunks;
+};
+
+__device__ __forceinline__ void job_coords(int job, const Sched &sp, int &l, int &tm, int &tn) {
+  l = job / sp.tiles;
+  int t = job - l * sp.tiles;
+  constexpr int GM = 8;  // tile rows per raster group (L2 reuse of B tiles)
+  int group = t / (GM * sp.tiles_n);
+  int first = group * GM;
+  int rows_in = min(GM, sp.tiles_m - first);
+  int w = t - group * GM * sp.tiles_n;
+  tm = first + w % rows_in;
+  tn = w / rows_in;
+}
+
+// The unit sequence every role walks: (job, chunk, TMEM buffer).
+template <int KIND, typename F>
+__device__ __forceinline__ void for_each_unit(const Sched &sp, F &&f) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int cj = b < sp.njobs ? (sp.njobs - 1 - b) / G + 1 : 0;
+  if (KIND == 0) {
+    for (int q = 0; q < cj; q += 2) {
+      const int nj = min(2, cj - q);
+      for (int c = 0; c < sp.nchunks; c++)
+        for (int s = 0; s < nj; s++)
+          if (!f(b + (q + s) * G, c, s)) return;
+    }
+  } else {
+    int u = 0;
+    for (int q = 0; q < cj; q++)
+      for (int c = 0; c < sp.nchunks; c++, u++)
+        if (!f(b + q * G, c, u & 1)) return;
+  }
+}
+
+__device__ __forceinline__ void set_status(int *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              const Sched sp, const GemmConsts gc, void *__restrict__ out, int ldo,
+              int32_t *__restrict__ rowmax, int32_t *__restrict__ colmax, int *status) {
+  using C = Cfg<KIND>;
+  constexpr int BN = C::BN, STAGES = C::STAGES;
+  constexpr uint32_t A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2;
+  constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  uint64_t *full = bars, *empty = bars + STAGES;
+  uint64_t *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 2, *mma_done = acc_empty + 2;
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(mma_done + 1);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiThreads);
+    }
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_par = 0;  // per stage: ever used / parity of its last load
+      for_each_unit<KIND>(sp, [&](int job, int c, int) -> bool {
+        int l, tm, tn;
+        job_coords(job, sp, l, tm, tn);
+        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        for (int kb = kb0; kb < kb1; kb++) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, kWaitLimit)) {
+            *s_abort = 1;
+            set_status(status, OS2_ERR_TIMEOUT);
+            return false;
+          }
+          mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+          tma_load_3d(sA + stage * A_BYTES, &mapA, &full[stage], kb * BK, tm * BM, l);
+          tma_load_3d(sB + stage * B_BYTES, &mapB, &full[stage], kb * BK, tn * BN, l);
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        return true;
+      });
+      // let every issued copy land before the CTA can exit
+      for (int s = 0; s < STAGES; s++)
+        if (used >> s & 1) {
+          volatile int no_abort = 0;
+          mbar_wait_bounded(&full[s], (last_par >> s) & 1, &no_abort, kWaitLimit);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t aphase[2] = {0, 0};
+      for_each_unit<KIND>(sp, [&](int, int c, int buf) -> bool {
+        if (!mbar_wait_bounded(&acc_empty[buf], aphase[buf] ^ 1, s_abort, kWaitLimit)) {
+          *s_abort = 1;
+          set_status(status, OS2_ERR_TIMEOUT);
+          return false;
+        }
+        aphase[buf] ^= 1;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        for (int kb = kb0; kb < kb1; kb++) {
+          if (!mbar_wait_bounded(&full[stage], phase, s_abort, kWaitLimit)) {
+            *s_abort = 1;
+            set_status(status, OS2_ERR_TIMEOUT);
+            return false;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k128(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bd = sdesc_k128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; kk++) {
+            const uint32_t acc = (kb > kb0 || kk > 0 || (KIND == 0 && c > 0)) ? 1u : 0u;
+            umma_f16(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);  // +32 bytes along k
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        umma_commit(&acc_full[buf]);
+        return true;
+      });
+      umma_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(mma_done, 0, &no_abort, kWaitLimit);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int r_in_tile = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    uint32_t aphase[2] = {0, 0};
+    if (KIND == 0) {
+      int8_t *outp = reinterpret_cast<int8_t *>(out);
+      for_each_unit<KIND>(sp, [&](int job, int c, int buf) -> bool {
+        // every lane waits (acquire), then the warp reconverges on one verdict
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], aphase[buf],
+                                                                   s_abort, kWaitLimit));
+        if (!ok) {
+          *s_abort = 1;
+          set_status(status, OS2_ERR_TIMEOUT);
+          return false;
+        }
+        aphase[buf] ^= 1;
+        tc_fence_after();
+        int l, tm, tn;
+        job_coords(job, sp, l, tm, tn);
+        const float p = gc.p[l], invp = gc.invp[l];
+        const uint32_t taddr = lane_base + (uint32_t)(buf * BN);
+        if (c != sp.nchunks - 1) {
+          // intermediate: subtract the nearest multiple of p, keep |r| <= ~0.52 p
+#pragma unroll 1
+          for (int g = 0; g < BN / 32; g++) {
+            uint32_t v[32];
+            tmem_ld32(taddr + g * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+              float x = __uint_as_float(v[i]);
+              v[i] = __float_as_uint(fmaf(-p, rintf(x * invp), x));
+            }
+            tmem_st32(taddr + g * 32, v);
+          }
+          tmem_wait_st();
+        } else {
+          // final: canonical symmetric residue, int8 store
+          const float hi = gc.hi[l], lo = gc.lo[l];
+          const int grow = tm * BM + r_in_tile;
+          const int col0 = tn * BN;
+          int8_t *dst = outp + ((size_t)l * sp.m + grow) * (size_t)ldo + col0;
+#pragma unroll 1
+          for (int g = 0; g < BN / 32; g++) {
+            uint32_t v[32];
+            tmem_ld32(taddr + g * 32, v);
+            tmem_wait_ld();
+            uint32_t packed[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) packed[i] = 0;
+#pragma unroll
+            for (int i = 0; i < 32; i++) {
+              float x = __uint_as_float(v[i]);
+              float r = fmaf(-p, rintf(x * invp), x);
+              r = r > hi ? r - p : r;
+              r = r < lo ? r + p : r;
+              packed[i >> 2] |= ((uint32_t)(int)r & 0xFFu) << (8 * (i & 3));
+            }
+            if (grow < sp.m) {
+              const int cb = col0 + g * 32;
+              if (cb + 32 <= sp.n) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + g * 32);
+                d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              } else {
+                for (int i = 0; i < 32 && cb + i < sp.n; i++)
+                  dst[g * 32 + i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        return true;
+      });
+    } else {
+      int32_t *outp = reinterpret_cast<int32_t *>(out);
+      int acc[BN];
+#pragma unroll
+      for (int i = 0; i < BN; i++) acc[i] = 0;
+      for_each_unit<KIND>(sp, [&](int job, int c, int buf) -> bool {
+        // every lane waits (acquire), then the warp reconverges on one verdict
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], aphase[buf],
+                                                                   s_abort, kWaitLimit));
+        if (!ok) {
+          *s_abort = 1;
+          set_status(status, OS2_ERR_TIMEOUT);
+          return false;
+        }
+        aphase[buf] ^= 1;
+        tc_fence_after();
+        const uint32_t taddr = lane_base + (uint32_t)(buf * BN);
+#pragma unroll
+        for (int g = 0; g < BN / 32; g++) {
+          uint32_t v[32];
+          tmem_ld32(taddr + g * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            int x = __float2int_rn(__uint_as_float(v[i]));
+            acc[g * 32 + i] = (c == 0) ? x : acc[g * 32 + i] + x;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[buf]);
+        if (c == sp.nchunks - 1) {
+          int l, tm, tn;
+          job_coords(job, sp, l, tm, tn);
+          const int grow = tm * BM + r_in_tile;
+          const int col0 = tn * BN;
+          if (outp && grow < sp.m) {
+            int32_t *dst = outp + ((size_t)l * sp.m + grow) * (size_t)ldo + col0;
+            if (col0 + BN <= sp.n) {
+#pragma unroll
+              for (int i = 0; i < BN; i += 4)
+                *reinterpret_cast<int4 *>(dst + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN; i++)
+                if (col0 + i < sp.n) dst[i] = acc[i];
+            }
+          }
+          if (rowmax) {
+            int mx = 0;
+#pragma unroll
+            for (int i = 0; i < BN; i++) mx = max(mx, acc[i]);
+            if (grow < sp.m) atomicMax(&rowmax[grow], mx);
+          }
+          if (colmax) {
+#pragma unroll
+            for (int i = 0; i < BN; i++) {
+              int v = __reduce_max_sync(0xffffffffu, acc[i]);
+              if (lane == 0 && col0 + i < sp.n) atomicMax(&colmax[col0 + i], v);
+            }
+          }
+        }
+        return true;
+      });
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// FP16 planes [nplanes][rows][kp]; box = 64 (k) x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, int kp, int rows, int nplanes, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kp, (cuuint64_t)rows, (cuuint64_t)nplanes};
+  cuuint64_t strides[2] = {(cuuint64_t)kp * 2, (cuuint64_t)kp * 2 * (cuuint64_t)rows};
+  cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  return v > 0 ? v : 1;
+}
+
+template <int KIND>
+cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
+                   int ldo, int32_t *rowmax, int32_t *colmax, int prod_bound_log2,
+                   const Os2Tables *t, int *status, cudaStream_t s) {
+  using C = Cfg<KIND>;
+  constexpr size_t smem = 1024 + (size_t)C::STAGES * (BM + C::BN) * BK * 2 + 256;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(k_gemm_tc<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, RA, kp, m, nplanes, BM) || !make_map(&mb, RB, kp, n, nplanes, C::BN))
+    return cudaErrorInvalidValue;
+  Sched sp;
+  sp.m = m;
+  sp.n = n;
+  sp.kb_total = kp / BK;
+  sp.tiles_m = (m + BM - 1) / BM;
+  sp.tiles_n = (n + C::BN - 1) / C::BN;
+  sp.tiles = sp.tiles_m * sp.tiles_n;
+  sp.njobs = sp.tiles * nplanes;
+  // k-blocks per chunk keep every FP32 partial sum an exact integer below 2^24
+  // (KIND 0 also carries a reduced remainder of magnitude <= 0.52 p + 1 <= 135).
+  const long long cap = (1LL << 24) - (KIND == 0 ? 135 : 0);
+  const long long per_block = (long long)BK << prod_bound_log2;
+  sp.chunk = (int)(cap / per_block);
+  if (sp.chunk < 1) return cudaErrorInvalidValue;
+  sp.nchunks = (sp.kb_total + sp.chunk - 1) / sp.chunk;
+  if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
+  const int grid = std::min(num_sms(), sp.njobs);
+  GemmConsts gc = t ? t->gemm : GemmConsts{};
+  k_gemm_tc<KIND><<<grid, kThreads, smem, s>>>(ma, mb, sp, gc, out, ldo, rowmax, colmax, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
+                           int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,
+                           int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s) {
+  if (m <= 0 || n <= 0 || kp <= 0) return cudaSuccess;
+  if (kind == 0)
+    return launch<0>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
+                     status, s);
+  return launch<1>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
+                   status, s);
+}

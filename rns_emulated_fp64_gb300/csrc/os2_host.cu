@@ -1,0 +1,484 @@
+// libos2 host side: the C ABI declared in include/os2.h, argument checking,
+// workspace layout, constant tables and the launch sequence of the five steps.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "os2_internal.cuh"
+
+// ---------------------------------------------------------------------------
+// Device status word (one per device); kernels receive its address.
+// ---------------------------------------------------------------------------
+__device__ int g_os2_status;
+
+int *os2_status_ptr() {
+  static std::mutex mu;
+  static int *ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_os2_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int *>(p);
+  }
+  return ptrs[dev];
+}
+
+// ---------------------------------------------------------------------------
+// Constant tables.  [Q] "256以下の法の選び方(手順2)" (moduli, footnote 6 order),
+// "秦九韶の大衍求一術" (M_l, inverses by the extended Euclidean algorithm,
+// use numbers W_l = M_l inv_l).
+// ---------------------------------------------------------------------------
+namespace {
+
+const int kModuli[OS2_MAX_MODULI] = {256, 255, 253, 251, 247, 241, 239, 233, 229, 227,
+                                     223, 217, 211, 199, 197, 193, 191, 181, 179, 173};
+
+struct U256 {
+  uint32_t w[8];
+};
+U256 u_from(uint32_t v) {
+  U256 r = {};
+  r.w[0] = v;
+  return r;
+}
+U256 u_mul(const U256 &a, uint32_t s) {
+  U256 r;
+  uint64_t c = 0;
+  for (int i = 0; i < 8; i++) {
+    c += (uint64_t)a.w[i] * s;
+    r.w[i] = (uint32_t)c;
+    c >>= 32;
+  }
+  return r;
+}
+U256 u_div(const U256 &a, uint32_t d, uint32_t *rem) {
+  U256 q;
+  uint64_t r = 0;
+  for (int i = 7; i >= 0; i--) {
+    uint64_t cur = (r << 32) | a.w[i];
+    q.w[i] = (uint32_t)(cur / d);
+    r = cur % d;
+  }
+  if (rem) *rem = (uint32_t)r;
+  return q;
+}
+U256 u_sub1(const U256 &a) {
+  U256 r = a;
+  for (int i = 0; i < 8; i++) {
+    if (r.w[i]--) break;
+  }
+  return r;
+}
+U256 u_shr1(const U256 &a) {
+  U256 r;
+  for (int i = 0; i < 8; i++) r.w[i] = (a.w[i] >> 1) | (i + 1 < 8 ? a.w[i + 1] << 31 : 0u);
+  return r;
+}
+int u_bitlen(const U256 &a) {
+  for (int i = 7; i >= 0; i--)
+    if (a.w[i]) return 32 * i + 32 - __builtin_clz(a.w[i]);
+  return 0;
+}
+uint32_t limb16(const U256 &a, int v) { return (a.w[v / 2] >> (16 * (v % 2))) & 0xFFFFu; }
+
+// a^-1 mod p by the extended Euclidean algorithm (a, p coprime)
+int inv_mod(int a, int p) {
+  int r0 = p, r1 = ((a % p) + p) % p, t0 = 0, t1 = 1;
+  while (r1) {
+    int q = r0 / r1, tmp = r0 - q * r1;
+    r0 = r1;
+    r1 = tmp;
+    tmp = t0 - q * t1;
+    t0 = t1;
+    t1 = tmp;
+  }
+  return ((t0 % p) + p) % p;
+}
+
+int sym(int x, int p) {
+  int r = ((x % p) + p) % p;
+  return r >= (p + 1) / 2 ? r - p : r;
+}
+
+void build_tables(int N, Os2Tables *t) {
+  memset(t, 0, sizeof(*t));
+  t->N = N;
+  U256 P = u_from(1);
+  for (int l = 0; l < N; l++) P = u_mul(P, (uint32_t)kModuli[l]);
+  const U256 H = u_shr1(u_sub1(P));  // floor((P-1)/2)
+  const U256 half = u_shr1(P);       // P/2 (P is even: 256 is a modulus)
+  t->res.N = t->crt.N = t->gemm.N = N;
+  for (int l = 0; l < N; l++) {
+    const int p = kModuli[l];
+    t->p[l] = p;
+    uint32_t rem = 0;
+    const U256 M = u_div(P, (uint32_t)p, nullptr);
+    u_div(M, (uint32_t)p, &rem);
+    t->inv[l] = inv_mod((int)rem, p);
+    const U256 W = u_mul(M, (uint32_t)t->inv[l]);
+    const float fp = (float)p, hi = (float)((p + 1) / 2 - 1), lo = (float)(-(p / 2));
+    t->res.p[l] = t->gemm.p[l] = fp;
+    t->res.invp[l] = t->gemm.invp[l] = 1.0f / fp;
+    t->res.hi[l] = t->gemm.hi[l] = hi;
+    t->res.lo[l] = t->gemm.lo[l] = lo;
+    int pw = 1;
+    for (int u = 0; u < 7; u++) {
+      t->res.w12[l][u] = (float)sym(pw, p);
+      pw = (int)(((long long)pw * 4096) % p);
+    }
+    t->crt.phi[l] = (float)((double)t->inv[l] / (double)p);
+    for (int v = 0; v < OS2_CRT_LIMBS; v++) t->crt.W16[l][v] = (int32_t)limb16(W, v);
+  }
+  for (int v = 0; v < OS2_CRT_LIMBS; v++) {
+    t->crt.P16[v] = (int32_t)limb16(P, v);
+    t->crt.half16[v] = (int32_t)limb16(half, v);
+  }
+  for (int i = 0; i < OS2_H_LIMBS; i++) t->res.H[i] = H.w[i];
+  t->res.bitlenH = u_bitlen(H);
+}
+
+std::atomic<int> g_variant{OS2_GEMM_TC};
+
+}  // namespace
+
+const Os2Tables *os2_tables(int N) {
+  static Os2Tables tabs[OS2_MAX_MODULI + 1];
+  static std::once_flag once;
+  if (N < 1 || N > OS2_MAX_MODULI) return nullptr;
+  std::call_once(once, [] {
+    for (int n = 1; n <= OS2_MAX_MODULI; n++) build_tables(n, &tabs[n]);
+  });
+  return &tabs[N];
+}
+
+// ---------------------------------------------------------------------------
+// Workspace layout
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxK = 1 << 17;
+
+struct Layout {
+  size_t e, f, EA, EB, R, K, planesA, planesB, cres, total;
+  int kp, ldcres;
+};
+
+bool make_layout(int m, int n, int k, int N, int mode, Layout *L) {
+  if (m < 0 || n < 0 || k < 0 || N < 1 || N > OS2_MAX_MODULI) return false;
+  if (mode != OS2_MODE_FAST && mode != OS2_MODE_ACCURATE) return false;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += os2_round_up(bytes, 256);
+    return o;
+  };
+  L->kp = (int)os2_round_up((size_t)std::max(k, 1), OS2_KP_ALIGN);
+  L->ldcres = (int)os2_round_up((size_t)std::max(n, 1), OS2_CRES_ALIGN);
+  L->e = take(4 * (size_t)m);
+  L->f = take(4 * (size_t)n);
+  if (mode == OS2_MODE_ACCURATE) {
+    L->EA = take(4 * (size_t)m);
+    L->EB = take(4 * (size_t)n);
+    L->R = take(4 * (size_t)m);
+    L->K = take(4 * (size_t)n);
+  } else {
+    L->EA = L->EB = L->R = L->K = 0;
+  }
+  L->planesA = take((size_t)N * m * L->kp * 2);
+  L->planesB = take((size_t)N * n * L->kp * 2);
+  L->cres = take((size_t)N * m * L->ldcres);
+  L->total = off;
+  return true;
+}
+
+os2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OS2_OK : OS2_ERR_CUDA; }
+
+template <typename T>
+T *at(void *ws, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+os2_status check_gemm_args(int m, int n, int k, const double *A, int lda, const double *B,
+                           int ldb, const double *C, int ldc, int N, int mode) {
+  if (m < 0 || n < 0 || k < 0) return OS2_ERR_INVALID_ARG;
+  if (N < 1 || N > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
+  if (mode != OS2_MODE_FAST && mode != OS2_MODE_ACCURATE) return OS2_ERR_INVALID_ARG;
+  if (lda < std::max(k, 1) || ldb < std::max(k, 1) || ldc < std::max(n, 1))
+    return OS2_ERR_INVALID_ARG;
+  if (k >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if (m > 0 && n > 0 && !C) return OS2_ERR_INVALID_ARG;
+  if (m > 0 && k > 0 && !A) return OS2_ERR_INVALID_ARG;
+  if (n > 0 && k > 0 && !B) return OS2_ERR_INVALID_ARG;
+  if ((A && !aligned(A, 8)) || (B && !aligned(B, 8)) || (C && !aligned(C, 8)))
+    return OS2_ERR_INVALID_ARG;
+  return OS2_OK;
+}
+
+// The five steps on device operands; arguments already checked.
+os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                    double *C, int ldc, int N, int mode, void *ws, const Layout &L,
+                    cudaStream_t s) {
+  if (m == 0 || n == 0) return OS2_OK;
+  if (k == 0) return cuda_status(cudaMemset2DAsync(C, (size_t)ldc * 8, 0, (size_t)n * 8, m, s));
+  const Os2Tables *t = os2_tables(N);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  int32_t *e = at<int32_t>(ws, L.e), *f = at<int32_t>(ws, L.f);
+  void *pa = at<void>(ws, L.planesA), *pb = at<void>(ws, L.planesB);
+  int8_t *cres = at<int8_t>(ws, L.cres);
+  cudaError_t err;
+  if (mode == OS2_MODE_FAST) {
+    // steps 1 + 2 fused: exponents from the revised bound, then residue planes
+    if ((err = launch_scale_residue(SM_FAST_FUSED, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
+      return cuda_status(err);
+    if ((err = launch_scale_residue(SM_FAST_FUSED, B, ldb, n, k, L.kp, f, nullptr, pb, t, status, s)))
+      return cuda_status(err);
+  } else {
+    // step 1, accurate: magnitude planes (aliasing the residue planes), one
+    // exact bound product with fused row/column maxima, exponents; then step 2
+    int32_t *EA = at<int32_t>(ws, L.EA), *EB = at<int32_t>(ws, L.EB);
+    int32_t *R = at<int32_t>(ws, L.R), *K = at<int32_t>(ws, L.K);
+    if ((err = launch_scale_residue(SM_BARS, A, lda, m, k, L.kp, nullptr, EA, pa, t, status, s)))
+      return cuda_status(err);
+    if ((err = launch_scale_residue(SM_BARS, B, ldb, n, k, L.kp, nullptr, EB, pb, t, status, s)))
+      return cuda_status(err);
+    if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
+    if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
+    if ((err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
+      return cuda_status(err);
+    if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
+    if ((err = launch_accu_exponents(K, EB, n, f, t, s))) return cuda_status(err);
+    if ((err = launch_scale_residue(SM_RESIDUES, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
+      return cuda_status(err);
+    if ((err = launch_scale_residue(SM_RESIDUES, B, ldb, n, k, L.kp, f, nullptr, pb, t, status, s)))
+      return cuda_status(err);
+  }
+  // step 3
+  if (g_variant.load() == OS2_GEMM_SIMT)
+    err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
+  else
+    err = launch_gemm_tc(0, m, n, L.kp, pa, pb, N, cres, L.ldcres, nullptr, nullptr, 14, t,
+                         status, s);
+  if (err) return cuda_status(err);
+  // steps 4 + 5
+  return cuda_status(launch_crt(m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+size_t os2_workspace_size(int m, int n, int k, int num_moduli, int mode) {
+  Layout L;
+  return make_layout(m, n, k, num_moduli, mode, &L) ? L.total : 0;
+}
+
+os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                    double *C, int ldc, int num_moduli, int mode, void *workspace,
+                    size_t workspace_bytes, void *stream) {
+  os2_status st = check_gemm_args(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode);
+  if (st) return st;
+  Layout L;
+  make_layout(m, n, k, num_moduli, mode, &L);
+  if (m > 0 && n > 0 && k > 0) {
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
+      return OS2_ERR_WORKSPACE;
+  }
+  return run_gemm(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
+                  static_cast<cudaStream_t>(stream));
+}
+
+size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode) {
+  Layout L;
+  if (!make_layout(m, n, k, num_moduli, mode, &L)) return 0;
+  return L.total + os2_round_up(8 * (size_t)m * k, 256) + os2_round_up(8 * (size_t)n * k, 256) +
+         os2_round_up(8 * (size_t)m * n, 256);
+}
+
+os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                         double *C, int ldc, int num_moduli, int mode, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  os2_status st = check_gemm_args(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode);
+  if (st) return st;
+  Layout L;
+  make_layout(m, n, k, num_moduli, mode, &L);
+  const size_t need = os2_host_workspace_size(m, n, k, num_moduli, mode);
+  if (m == 0 || n == 0) return OS2_OK;
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return OS2_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  double *dA = at<double>(workspace, L.total);
+  double *dB = at<double>(workspace, L.total + os2_round_up(8 * (size_t)m * k, 256));
+  double *dC = at<double>(workspace, L.total + os2_round_up(8 * (size_t)m * k, 256) +
+                                          os2_round_up(8 * (size_t)n * k, 256));
+  const int kk = std::max(k, 1);
+  cudaError_t err;
+  if (k > 0) {
+    if ((err = cudaMemcpy2DAsync(dA, 8 * (size_t)k, A, 8 * (size_t)lda, 8 * (size_t)k, m,
+                                 cudaMemcpyHostToDevice, s)))
+      return cuda_status(err);
+    if ((err = cudaMemcpy2DAsync(dB, 8 * (size_t)k, B, 8 * (size_t)ldb, 8 * (size_t)k, n,
+                                 cudaMemcpyHostToDevice, s)))
+      return cuda_status(err);
+  }
+  st = run_gemm(m, n, k, dA, kk, dB, kk, dC, n, num_moduli, mode, workspace, L, s);
+  if (st) return st;
+  return cuda_status(cudaMemcpy2DAsync(C, 8 * (size_t)ldc, dC, 8 * (size_t)n, 8 * (size_t)n, m,
+                                       cudaMemcpyDeviceToHost, s));
+}
+
+os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                     int num_moduli, int mode, int32_t *e, int32_t *f, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  if (m < 0 || n < 0 || k < 0) return OS2_ERR_INVALID_ARG;
+  if (lda < std::max(k, 1) || ldb < std::max(k, 1)) return OS2_ERR_INVALID_ARG;
+  if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
+  if (mode != OS2_MODE_FAST && mode != OS2_MODE_ACCURATE) return OS2_ERR_INVALID_ARG;
+  if (k >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if ((m && (!e || (k && !A))) || (n && (!f || (k && !B)))) return OS2_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Os2Tables *t = os2_tables(num_moduli);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  cudaError_t err;
+  if (k == 0) {
+    if (m && (err = cudaMemsetAsync(e, 0, 4 * (size_t)m, s))) return cuda_status(err);
+    if (n && (err = cudaMemsetAsync(f, 0, 4 * (size_t)n, s))) return cuda_status(err);
+    return OS2_OK;
+  }
+  if (mode == OS2_MODE_FAST) {
+    if ((err = launch_scale_residue(SM_FAST_SCALE, A, lda, m, k, 0, e, nullptr, nullptr, t, status, s)))
+      return cuda_status(err);
+    return cuda_status(
+        launch_scale_residue(SM_FAST_SCALE, B, ldb, n, k, 0, f, nullptr, nullptr, t, status, s));
+  }
+  Layout L;
+  make_layout(m, n, k, 1, mode, &L);
+  if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return OS2_ERR_WORKSPACE;
+  int32_t *EA = at<int32_t>(workspace, L.EA), *EB = at<int32_t>(workspace, L.EB);
+  int32_t *R = at<int32_t>(workspace, L.R), *K = at<int32_t>(workspace, L.K);
+  void *pa = at<void>(workspace, L.planesA), *pb = at<void>(workspace, L.planesB);
+  if ((err = launch_scale_residue(SM_BARS, A, lda, m, k, L.kp, nullptr, EA, pa, t, status, s)))
+    return cuda_status(err);
+  if ((err = launch_scale_residue(SM_BARS, B, ldb, n, k, L.kp, nullptr, EB, pb, t, status, s)))
+    return cuda_status(err);
+  if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)std::max(m, 1), s))) return cuda_status(err);
+  if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)std::max(n, 1), s))) return cuda_status(err);
+  if (m > 0 && n > 0 &&
+      (err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
+    return cuda_status(err);
+  if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
+  return cuda_status(launch_accu_exponents(K, EB, n, f, t, s));
+}
+
+os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t *exps,
+                        int num_moduli, void *planes, int ldp, void *stream) {
+  if (rows < 0 || k < 0 || ldx < std::max(k, 1)) return OS2_ERR_INVALID_ARG;
+  if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
+  if (ldp < k || ldp % OS2_KP_ALIGN) return OS2_ERR_INVALID_ARG;
+  if (k >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if (rows == 0 || ldp == 0) return OS2_OK;
+  if ((k && !X) || !exps || !planes || !aligned(planes, 16)) return OS2_ERR_INVALID_ARG;
+  const Os2Tables *t = os2_tables(num_moduli);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  return cuda_status(launch_scale_residue(SM_RESIDUES, X, ldx, rows, k, ldp,
+                                          const_cast<int32_t *>(exps), nullptr, planes, t, status,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB, int ldp,
+                             int num_moduli, int out_kind, void *out, int ldo, int variant,
+                             void *stream) {
+  if (m < 0 || n < 0 || k < 0 || k > ldp || ldp % OS2_KP_ALIGN) return OS2_ERR_INVALID_ARG;
+  if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
+  if (out_kind != OS2_OUT_MODP_INT8 && out_kind != OS2_OUT_RAW_INT32) return OS2_ERR_INVALID_ARG;
+  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT) return OS2_ERR_INVALID_ARG;
+  if (ldo < std::max(n, 1)) return OS2_ERR_INVALID_ARG;
+  if (out_kind == OS2_OUT_MODP_INT8 && ldo % OS2_CRES_ALIGN) return OS2_ERR_INVALID_ARG;
+  if (out_kind == OS2_OUT_RAW_INT32 && ldo % 4) return OS2_ERR_INVALID_ARG;
+  if (ldp >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if (m == 0 || n == 0) return OS2_OK;
+  if (!out || !aligned(out, 16)) return OS2_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ldp == 0) {
+    const size_t es = out_kind == OS2_OUT_RAW_INT32 ? 4 : 1;
+    return cuda_status(
+        cudaMemsetAsync(out, 0, es * (size_t)num_moduli * m * ldo, s));
+  }
+  if (!RA || !RB || !aligned(RA, 16) || !aligned(RB, 16)) return OS2_ERR_INVALID_ARG;
+  const Os2Tables *t = os2_tables(num_moduli);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  if (variant == OS2_GEMM_SIMT)
+    return cuda_status(launch_gemm_simt(m, n, ldp, RA, RB, num_moduli, out_kind, out, ldo, t, s));
+  return cuda_status(launch_gemm_tc(out_kind == OS2_OUT_MODP_INT8 ? 0 : 1, m, n, ldp, RA, RB,
+                                    num_moduli, out, ldo, nullptr, nullptr, 14, t, status, s));
+}
+
+os2_status os2_crt(int m, int n, const int8_t *c, int ldcres, int num_moduli, const int32_t *e,
+                   const int32_t *f, double *C, int ldc, uint32_t *X_out, void *stream) {
+  if (m < 0 || n < 0 || ldcres < std::max(n, 1) || ldcres % 4 || ldc < std::max(n, 1))
+    return OS2_ERR_INVALID_ARG;
+  if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OS2_OK;
+  if (!c || !e || !f || !C || !aligned(c, 4) || !aligned(C, 8)) return OS2_ERR_INVALID_ARG;
+  const Os2Tables *t = os2_tables(num_moduli);
+  if (!t) return OS2_ERR_CUDA;
+  return cuda_status(launch_crt(m, n, c, ldcres, e, f, C, ldc, X_out, t,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+int os2_moduli(int num_moduli, int32_t *out) {
+  if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI || !out) return 0;
+  for (int l = 0; l < num_moduli; l++) out[l] = kModuli[l];
+  return num_moduli;
+}
+
+os2_status os2_get_status(void *stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OS2_ERR_CUDA;
+  int *p = os2_status_ptr();
+  if (!p) return OS2_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return OS2_ERR_CUDA;
+  if (v && cudaMemset(p, 0, sizeof(int)) != cudaSuccess) return OS2_ERR_CUDA;
+  return static_cast<os2_status>(v);
+}
+
+os2_status os2_set_gemm_variant(int variant) {
+  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT) return OS2_ERR_INVALID_ARG;
+  g_variant.store(variant);
+  return OS2_OK;
+}
+
+const char *os2_status_string(int status) {
+  switch (status) {
+    case OS2_OK: return "ok";
+    case OS2_ERR_INVALID_ARG: return "invalid argument";
+    case OS2_ERR_UNSUPPORTED: return "unsupported size or configuration";
+    case OS2_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case OS2_ERR_NONFINITE: return "non-finite input entry";
+    case OS2_ERR_RANGE: return "CRT range exceeded";
+    case OS2_ERR_TIMEOUT: return "device-side wait timed out";
+    case OS2_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
+  if (m <= 0 || n <= 0 || k < 0 || num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return 0;
+  if (k == 0) return 0;
+  return mode == OS2_MODE_ACCURATE ? 9 : 4;
+}
+
+}  // extern "C"

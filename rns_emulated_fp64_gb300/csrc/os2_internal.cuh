@@ -1,0 +1,88 @@
+// Internal declarations shared by the translation units of libos2.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/os2.h"
+
+#define OS2_MAX_MODULI 20
+#define OS2_KP_ALIGN 64          // residue-plane row pitch granularity (one 128-byte k-block)
+#define OS2_CRES_ALIGN 16        // int8 product-residue row pitch granularity
+#define OS2_H_LIMBS 7            // 32-bit limbs for H (P < 2^156 for N <= 20)
+#define OS2_CRT_LIMBS 10         // 16-bit limbs for the CRT sums (160 bits)
+
+// Step-2 constants (kernel parameter, lives in the constant bank).
+struct ResConsts {
+  int N;
+  float p[OS2_MAX_MODULI];       // p_l
+  float invp[OS2_MAX_MODULI];    // fl(1/p_l)
+  float hi[OS2_MAX_MODULI];      // ceil(p_l/2) - 1   (top of the symmetric range)
+  float lo[OS2_MAX_MODULI];      // -floor(p_l/2)     (bottom)
+  float w12[OS2_MAX_MODULI][7];  // symmetric residue of 2^(12 t) mod p_l, t = 0..6
+  uint32_t H[OS2_H_LIMBS];       // H = floor((P-1)/2), little-endian 32-bit limbs
+  int bitlenH;
+};
+
+// Steps 4-5 constants.
+struct CrtConsts {
+  int N;
+  float phi[OS2_MAX_MODULI];                      // fl(inv_l / p_l) = fl(W_l / P)
+  int32_t W16[OS2_MAX_MODULI][OS2_CRT_LIMBS];     // W_l = M_l inv_l in 16-bit limbs
+  int32_t P16[OS2_CRT_LIMBS];                     // P in 16-bit limbs
+  int32_t half16[OS2_CRT_LIMBS];                  // P/2 in 16-bit limbs
+};
+
+// Step-3 constants.
+struct GemmConsts {
+  int N;
+  float p[OS2_MAX_MODULI];
+  float invp[OS2_MAX_MODULI];
+  float hi[OS2_MAX_MODULI];
+  float lo[OS2_MAX_MODULI];
+};
+
+struct Os2Tables {
+  int N;
+  int32_t p[OS2_MAX_MODULI];
+  int32_t inv[OS2_MAX_MODULI];
+  ResConsts res;
+  CrtConsts crt;
+  GemmConsts gemm;
+};
+
+// Host: tables for N moduli (cached; thread-safe).  NULL on bad N.
+const Os2Tables *os2_tables(int N);
+
+// Per-device status word (device address), set up on first use.
+int *os2_status_ptr();
+
+// Row-scale / residue kernel modes.
+enum ScaleMode {
+  SM_FAST_FUSED = 0,   // e from the revised fast bound, then residue planes
+  SM_RESIDUES = 1,     // residue planes with given exponents
+  SM_FAST_SCALE = 2,   // e only
+  SM_BARS = 3,         // accurate mode: E_i and the 7-bit magnitude plane
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_scale_residue(int mode, const double *X, long ldx, int rows, int k, int kp,
+                                 int32_t *e, int32_t *E, void *planes, const Os2Tables *t,
+                                 int *status, cudaStream_t s);
+cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,
+                                  const Os2Tables *t, cudaStream_t s);
+cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t *e,
+                       const int32_t *f, double *C, int ldc, uint32_t *X_out, const Os2Tables *t,
+                       cudaStream_t s);
+cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *RB, int N,
+                             int out_kind, void *out, int ldo, const Os2Tables *t, cudaStream_t s);
+
+// tcgen05 GEMM.  kind: 0 = mod-p int8 output, 1 = exact int32 (raw output and/or
+// row/col maxima).  prod_bound_log2: log2 of the largest |a*b| of one term
+// (14 for residues, 12 for the accurate-mode magnitude planes).
+cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
+                           int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,
+                           int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s);
+
+static inline size_t os2_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

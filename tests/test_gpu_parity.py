@@ -1,0 +1,332 @@
+"""Parity of every step of the CUDA path against the CPU oracle, through the
+C ABI.  Integer results (exponents, residue planes, raw products, residue
+products, CRT integers) must be bit-exact; FP64 results must be bit-identical
+to the oracle's correctly rounded values, which implies the stated bound
+|dC_ij| <= 2^-50 (|A||B|)_ij (checked as well)."""
+import numpy as np
+import pytest
+import torch
+
+import rns_emulated_fp64_gb300 as os2
+import workloads
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TOL = 2.0 ** -50
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV)
+
+
+def status_ok():
+    st = os2.get_status()
+    assert st == 0, os2.status_string(st)
+
+
+def assert_bits_equal(got, want, what):
+    got = np.ascontiguousarray(got, np.float64)
+    want = np.ascontiguousarray(want, np.float64)
+    bad = np.flatnonzero(got.view(np.uint64) != want.view(np.uint64))
+    assert bad.size == 0, f"{what}: {bad.size} entries differ, first {bad[:5]}: " \
+                          f"{got.ravel()[bad[:5]]} vs {want.ravel()[bad[:5]]}"
+
+
+def check_tolerance(C, A, Bt, rows, cols, ref):
+    absprod = np.abs(A[rows]) @ np.abs(Bt[cols]).T
+    assert np.all(np.abs(C - ref) <= TOL * absprod)
+
+
+SHAPES = [(64, 64, 64), (1, 1, 1), (3, 5, 7), (129, 257, 65), (300, 520, 1000), (128, 256, 960),
+          (130, 140, 1921)]
+
+
+# ------------------------------------------------------------------ step 1 --
+@pytest.mark.parametrize("kind,phi", [("normal", 0.0), ("spread", 0.5), ("spread", 4.0)])
+@pytest.mark.parametrize("N", [2, 12, 16, 20])
+def test_scale_fast_parity(kind, phi, N):
+    A, Bt = workloads.make_pair(kind, 257, 130, 777, seed=N, phi=phi)
+    A[5] = 0.0
+    A[7, ::3] = 5e-324
+    e, f = os2.scale(dev(A), dev(Bt), N, "fast")
+    status_ok()
+    assert np.array_equal(e.cpu().numpy(), orc.scale_fast(A, N))
+    assert np.array_equal(f.cpu().numpy(), orc.scale_fast(Bt, N))
+
+
+@pytest.mark.parametrize("N", [4, 14, 20])
+def test_scale_accurate_parity(N):
+    A, Bt = workloads.make_pair("spread", 200, 150, 333, seed=N, phi=2.0)
+    Bt[3] = 0.0
+    e, f = os2.scale(dev(A), dev(Bt), N, "accurate")
+    status_ok()
+    ee, ff = orc.scale_accu(A, Bt, N)
+    assert np.array_equal(e.cpu().numpy(), ee)
+    assert np.array_equal(f.cpu().numpy(), ff)
+
+
+# ------------------------------------------------------------------ step 2 --
+@pytest.mark.parametrize("N", [1, 7, 16, 20])
+@pytest.mark.parametrize("kind,phi", [("spread", 4.0), ("normal", 0.0)])
+def test_residue_planes_parity(N, kind, phi):
+    A, _ = workloads.make_pair(kind, 67, 1, 301, seed=3, phi=phi)
+    A[2, 0] = -2.0 ** 1000
+    A[4, :] = 0.0
+    e = orc.scale_fast(A, N)
+    planes = os2.residues(dev(A), dev(e), N)
+    status_ok()
+    got = planes.cpu().numpy()
+    assert got.shape == (N, 67, 320)
+    want = orc.residues(A, e, N)
+    assert np.array_equal(got[:, :, :301].astype(np.int64), want.astype(np.int64))
+    assert np.all(got[:, :, 301:] == 0)
+
+
+def test_residues_extreme_exponents():
+    """Exponents far from the fast-mode choice exercise every word of the
+    integer split (|A'| just below 2^84) and deep right shifts."""
+    rng = np.random.default_rng(11)
+    X = rng.standard_normal((40, 64))
+    E = int(np.frexp(np.abs(X).max())[1])          # |x| < 2^E
+    for N in (5, 20):
+        for e_val in (-60, -1, 0, 30, 83 - E):
+            e = np.full(40, e_val, np.int32)
+            planes = os2.residues(dev(X), dev(e), N)
+            status_ok()
+            want = orc.residues(X, e, N)
+            assert np.array_equal(planes.cpu().numpy()[:, :, :64].astype(np.int64),
+                                  want.astype(np.int64))
+
+
+# ------------------------------------------------------------------ step 3 --
+def _planes_pair(m, n, k, N, seed=0, kind="spread", phi=1.0):
+    A, Bt = workloads.make_pair(kind, m, n, k, seed=seed, phi=phi)
+    e = orc.scale_fast(A, N)
+    f = orc.scale_fast(Bt, N)
+    return A, Bt, e, f, os2.residues(dev(A), dev(e), N), os2.residues(dev(Bt), dev(f), N)
+
+
+def _int_product(RA, RB, k):
+    a = RA.float().cpu().numpy().astype(np.int64)[:, :, :k]
+    b = RB.float().cpu().numpy().astype(np.int64)[:, :, :k]
+    return np.einsum("lik,ljk->lij", a, b)
+
+
+@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_SIMT])
+@pytest.mark.parametrize("m,n,k", [(128, 128, 64), (129, 257, 65), (300, 200, 1100), (64, 64, 4097)])
+def test_raw_int32_products_bit_exact(variant, m, n, k):
+    N = 3
+    A, Bt, e, f, RA, RB = _planes_pair(m, n, k, N)
+    G = os2.gemm_residues(RA, RB, k, os2.OUT_RAW_INT32, variant)
+    status_ok()
+    want = _int_product(RA, RB, k)
+    assert np.array_equal(G.cpu().numpy()[:, :, :n].astype(np.int64), want)
+
+
+@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_SIMT])
+@pytest.mark.parametrize("m,n,k,N", [(128, 256, 64, 2), (129, 257, 65, 14), (300, 520, 1000, 16),
+                                     (256, 512, 2000, 20), (70, 33, 3000, 9)])
+def test_modp_products_bit_exact(variant, m, n, k, N):
+    A, Bt, e, f, RA, RB = _planes_pair(m, n, k, N, seed=m)
+    c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, variant)
+    status_ok()
+    rows = np.arange(m, dtype=np.int32)
+    cols = np.arange(n, dtype=np.int32)
+    ref = orc.gemm_entries(A, Bt, N, rows, cols, want_X=False, want_G=False)
+    got = np.transpose(c.cpu().numpy()[:, :, :n], (1, 2, 0))
+    assert np.array_equal(got, ref.c)
+
+
+def test_int32_accumulation_worst_case():
+    """[Q] 手順3: all residues -128 with the inner dimension just below 2^17
+    gives 2^14 (2^17 - 64) < 2^31, exact."""
+    k = (1 << 17) - 64
+    RA = torch.full((1, 128, k), -128.0, dtype=torch.float16, device=DEV)
+    RB = torch.full((1, 128, k), -128.0, dtype=torch.float16, device=DEV)
+    G = os2.gemm_residues(RA, RB, k, os2.OUT_RAW_INT32, os2.GEMM_TC)
+    status_ok()
+    assert torch.all(G[:, :, :128] == 16384 * k)
+    c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC)
+    status_ok()
+    assert torch.all(c[:, :, :128] == 0)       # 2^14 k is a multiple of 256
+
+
+def test_modp_alternating_extremes():
+    """Residues at the ends of every modulus range, products of alternating
+    sign: the in-TMEM reduction keeps every partial sum exact."""
+    N, m, n, k = 20, 128, 256, 4096
+    mods = os2.moduli(N)
+    rng = np.random.default_rng(5)
+    ra = np.zeros((N, m, k), np.float16)
+    rb = np.zeros((N, n, k), np.float16)
+    for l, p in enumerate(mods):
+        lo, hi = -(p // 2), (p + 1) // 2 - 1
+        ra[l] = rng.choice([lo, hi], size=(m, k))
+        rb[l] = rng.choice([lo, hi], size=(n, k))
+    RA, RB = dev(ra), dev(rb)
+    c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC).cpu().numpy()[:, :, :n]
+    status_ok()
+    G = np.einsum("lik,ljk->lij", ra.astype(np.int64), rb.astype(np.int64))
+    for l, p in enumerate(mods):
+        r = np.mod(G[l], p)
+        r = np.where(r >= (p + 1) // 2, r - p, r)
+        assert np.array_equal(c[l].astype(np.int64), r)
+
+
+# --------------------------------------------------------------- steps 4-5 --
+@pytest.mark.parametrize("N", [2, 12, 14, 16, 20])
+def test_crt_parity_from_oracle_residues(N):
+    A, Bt = workloads.make_pair("spread", 37, 45, 90, seed=N, phi=2.0)
+    ref = orc.gemm_entries(A, Bt, N)
+    cres = np.zeros((N, 37, 48), np.int8)
+    cres[:, :, :45] = np.transpose(ref.c, (2, 0, 1))
+    C, X = os2.crt(dev(cres), 45, dev(ref.e), dev(ref.f), want_X=True)
+    status_ok()
+    assert np.array_equal(X.cpu().numpy().view(np.uint32), ref.X)
+    assert_bits_equal(C.cpu().numpy(), ref.C, "C")
+
+
+def test_crt_random_residues_and_rounding():
+    """Arbitrary residue vectors (X anywhere in [-P/2, P/2)) and exponents that
+    push the result into the subnormal and overflow ranges."""
+    rng = np.random.default_rng(2)
+    for N in (1, 3, 16, 20):
+        mods = os2.moduli(N)
+        m, n = 33, 65
+        cres = np.zeros((N, m, 80), np.int8)
+        for l, p in enumerate(mods):
+            cres[l, :, :n] = rng.integers(-(p // 2), (p + 1) // 2, size=(m, n))
+        e = rng.integers(-1300, 1300, size=m).astype(np.int32)
+        f = rng.integers(-700, 700, size=n).astype(np.int32)
+        C, X = os2.crt(dev(cres), n, dev(e), dev(f), want_X=True)
+        status_ok()
+        Xn = X.cpu().numpy().view(np.uint32)
+        Cn = C.cpu().numpy()
+        P = int(np.prod([int(p) for p in mods], dtype=object))
+        for i in range(0, m, 4):
+            for j in range(0, n, 3):
+                res = [int(cres[l, i, j]) for l in range(N)]
+                x = orc.crt_small(res, mods) if P < 2 ** 62 else None
+                xv = orc.limbs_to_int(Xn[i, j])
+                assert -P // 2 <= xv < P // 2 + (P % 2)
+                for l, p in enumerate(mods):
+                    assert (xv - res[l]) % p == 0
+                if x is not None:
+                    assert xv == (x - P if x >= (P + 1) // 2 else x)
+                want = orc.round_scaled(xv, int(e[i]) + int(f[j]))
+                assert Cn[i, j] == want or (np.isinf(Cn[i, j]) and np.isinf(want))
+                assert np.signbit(Cn[i, j]) == np.signbit(want)
+
+
+# ------------------------------------------------------------- end to end --
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+@pytest.mark.parametrize("m,n,k", SHAPES)
+def test_gemm_end_to_end_small(mode, m, n, k):
+    N = 14
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=k, phi=1.0)
+    C = os2.gemm(dev(A), dev(Bt), N, mode).cpu().numpy()
+    status_ok()
+    ref = orc.gemm_entries(A, Bt, N, mode=orc.FAST if mode == "fast" else orc.ACCURATE,
+                           want_X=False, want_c=False, want_G=False)
+    assert ref.mismatches == 0
+    assert_bits_equal(C, ref.C, f"{mode} {m}x{n}x{k}")
+    check_tolerance(C, A, Bt, np.arange(m), np.arange(n), ref.C)
+
+
+def test_gemm_64cube_normal_config():
+    """64^3, N(0,1) from seed 0, 14 moduli, fast mode: every entry."""
+    A, Bt = workloads.make_pair("normal", 64, 64, 64, seed=0)
+    C = os2.gemm(dev(A), dev(Bt), 14, "fast").cpu().numpy()
+    status_ok()
+    ref = orc.gemm_entries(A, Bt, 14)
+    assert_bits_equal(C, ref.C, "64^3")
+
+
+def test_simt_variant_end_to_end():
+    A, Bt = workloads.make_pair("spread", 150, 170, 400, seed=1, phi=2.0)
+    try:
+        os2.set_gemm_variant(os2.GEMM_SIMT)
+        Cs = os2.gemm(dev(A), dev(Bt), 16).cpu().numpy()
+    finally:
+        os2.set_gemm_variant(os2.GEMM_TC)
+    Ct = os2.gemm(dev(A), dev(Bt), 16).cpu().numpy()
+    status_ok()
+    assert_bits_equal(Cs, Ct, "simt vs tc")
+    ref = orc.gemm_entries(A, Bt, 16, want_X=False, want_c=False, want_G=False)
+    assert_bits_equal(Ct, ref.C, "tc vs oracle")
+
+
+def test_integer_inputs_exact_on_gpu():
+    A, Bt = workloads.make_pair("int", 200, 300, 500, seed=4, phi=1000)
+    for mode in ("fast", "accurate"):
+        C = os2.gemm(dev(A), dev(Bt), 14, mode).cpu().numpy()
+        status_ok()
+        assert np.array_equal(C, A @ Bt.T)
+
+
+def test_edge_cases():
+    # k = 0 -> zeros; m or n = 0 -> nothing
+    A = torch.zeros((5, 0), dtype=torch.float64, device=DEV)
+    Bt = torch.zeros((3, 0), dtype=torch.float64, device=DEV)
+    C = torch.full((5, 3), 7.0, dtype=torch.float64, device=DEV)
+    os2.gemm(A, Bt, 14, out=C)
+    assert torch.all(C == 0)
+    os2.gemm(torch.zeros((0, 4), dtype=torch.float64, device=DEV),
+             torch.ones((3, 4), dtype=torch.float64, device=DEV), 14)
+    # zero rows / columns, subnormals, huge magnitudes, leading dimensions > k
+    rng = np.random.default_rng(8)
+    Abig = rng.standard_normal((70, 100))
+    Bbig = rng.standard_normal((90, 100))
+    Abig[3] = 0.0
+    Bbig[:, 7] = 0.0
+    Bbig[5] = 0.0
+    Abig[10] *= 2.0 ** -1060
+    Abig[11] *= 2.0 ** 900
+    Bbig[12] *= 2.0 ** 120
+    At = dev(Abig)[:, :77]
+    Btt = dev(Bbig)[:, :77]
+    for mode, om in (("fast", orc.FAST), ("accurate", orc.ACCURATE)):
+        Cg = os2.gemm(At, Btt, 16, mode).cpu().numpy()
+        status_ok()
+        ref = orc.gemm_entries(np.ascontiguousarray(Abig[:, :77]), np.ascontiguousarray(Bbig[:, :77]),
+                               16, mode=om, want_X=False, want_c=False, want_G=False)
+        assert_bits_equal(Cg, ref.C, f"edge {mode}")
+
+
+def test_nonfinite_input_sets_status():
+    A, Bt = workloads.make_pair("normal", 40, 40, 40)
+    A[3, 4] = np.nan
+    os2.gemm(dev(A), dev(Bt), 14)
+    assert os2.get_status() == os2.binding.ERR_NONFINITE
+    assert os2.get_status() == 0        # cleared
+    Bt[1, 1] = -np.inf
+    A[3, 4] = 1.0
+    os2.gemm(dev(A), dev(Bt), 14, "accurate")
+    assert os2.get_status() == os2.binding.ERR_NONFINITE
+
+
+@pytest.mark.parametrize("s", [-200, -100, -50, 50, 100, 200])
+def test_scale_invariance_on_gpu(s):
+    """[G] Methodik 2: A * 2^s gives C * 2^s exactly, in both modes; also with
+    B scaled (C * 2^2s)."""
+    A, Bt = workloads.make_pair("normal", 256, 192, 512, seed=0)
+    for mode in ("fast", "accurate"):
+        C0 = os2.gemm(dev(A), dev(Bt), 16, mode).cpu().numpy()
+        Cs = os2.gemm(dev(np.ldexp(A, s)), dev(Bt), 16, mode).cpu().numpy()
+        Css = os2.gemm(dev(np.ldexp(A, s)), dev(np.ldexp(Bt, s)), 16, mode).cpu().numpy()
+        status_ok()
+        assert_bits_equal(Cs, np.ldexp(C0, s), f"A*2^{s}")
+        assert_bits_equal(Css, np.ldexp(C0, 2 * s), f"A,B*2^{s}")
+
+
+def test_host_entry_point_matches_device():
+    A, Bt = workloads.make_pair("spread", 100, 120, 300, seed=6, phi=2.0)
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(Bt).pin_memory()
+    Ch = torch.empty((100, 120), dtype=torch.float64).pin_memory()
+    os2.gemm_host(Ah, Bh, Ch, 14)
+    torch.cuda.synchronize()
+    status_ok()
+    Cd = os2.gemm(dev(A), dev(Bt), 14).cpu().numpy()
+    assert_bits_equal(Ch.numpy(), Cd, "host vs device entry")
