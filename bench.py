@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Benchmark of the Ozaki Scheme II emulated DGEMM on GB300.
+
+Metric: emulated-DGEMM TFLOP/s = 2 m n k / t for C = A B with m = n = k = 8192,
+entries (U(0,1) - 0.5) exp(0.5 N(0,1)) (seed = rank), 16 moduli, revised fast
+mode.  One step = one os2_gemm call (all five steps of the method) with the
+inputs already resident in HBM; `e2e` is the same metric through
+os2_gemm_host with the inputs and the result in pinned host memory (copies
+inside the timed region).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank multiplies its own independent pair of
+matrices (no collective on the data path; weak scaling), timing is bracketed
+by barriers and the max over ranks is reported.
+
+`--impl reference` times the CPU oracle (the exact reference implementation of
+the method) on the host cores, on a bounded sample of output entries of the
+same workload; only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "emulated-DGEMM TFLOP/s (2mnk/t) at 8192^3 & INT8 tensor-pipe utilisation"
+UNIT = "TFLOP/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--m", type=int, default=8192)
+    ap.add_argument("--n", type=int, default=8192)
+    ap.add_argument("--k", type=int, default=8192)
+    ap.add_argument("--num-moduli", type=int, default=16)
+    ap.add_argument("--mode", default="fast", choices=["fast", "accurate"])
+    ap.add_argument("--phi", type=float, default=0.5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-context", action="store_true", help="skip native DGEMM / accuracy context")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def workload_name(a):
+    return (f"{a.m}x{a.n}x{a.k} FP64 GEMM, entries (U(0,1)-0.5)*exp({a.phi}*N(0,1)), "
+            f"{a.num_moduli} moduli, {a.mode} mode")
+
+
+def config(a, extra=None):
+    c = {"workload": workload_name(a), "m": a.m, "n": a.n, "k": a.k, "num_moduli": a.num_moduli,
+         "mode": a.mode, "phi": a.phi, "seed": "rank",
+         "l2": ("inputs larger than L2 (A and B %d MiB each), no flush" % (a.m * a.k * 8 >> 20))
+         if a.m * a.k * 8 > 129e6 else "inputs smaller than L2 (no flush): small-case run"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", uuid], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- utilities --
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's
+    source is unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        d = json.load(fh).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, d["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if h != d["source_sha256"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+def exact_dot(a, b):
+    """Correctly rounded sum_h a_h b_h (Dekker products + math.fsum)."""
+    p = a * b
+    c = 134217729.0
+
+    def split(x):
+        t = c * x
+        hi = t - (t - x)
+        return hi, x - hi
+
+    ah, al = split(a)
+    bh, bl = split(b)
+    err = ((ah * bh - p) + ah * bl + al * bh) + al * bl
+    return math.fsum(np.concatenate([p, err]).tolist())
+
+
+def dist_setup(a):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle ---
+def oracle_sample(A, Bt, a, seconds, rows_cols=None):
+    """Time the oracle on a growing grid of output entries until `seconds`
+    of work is reached; returns (entries, elapsed, result)."""
+    from oracle import oracle as orc
+    mode = orc.FAST if a.mode == "fast" else orc.ACCURATE
+    m, n = A.shape[0], Bt.shape[0]
+    if rows_cols is not None:
+        rows, cols = rows_cols
+        t0 = time.perf_counter()
+        ref = orc.gemm_entries(A, Bt, a.num_moduli, rows, cols, mode=mode, want_X=False,
+                               want_c=False, want_G=False)
+        return len(rows) * len(cols), time.perf_counter() - t0, ref, (rows, cols)
+    side = 4
+    while True:
+        rows, cols = workloads.sample_grid(m, n, side, seed=1)
+        t0 = time.perf_counter()
+        ref = orc.gemm_entries(A, Bt, a.num_moduli, rows, cols, mode=mode, want_X=False,
+                               want_c=False, want_G=False)
+        dt = time.perf_counter() - t0
+        if dt >= seconds * 0.5 or side >= min(m, n):
+            return len(rows) * len(cols), dt, ref, (rows, cols)
+        grow = math.sqrt(seconds / max(dt, 1e-3))
+        side = int(min(min(m, n), max(side * 2, side * min(grow, 8))))
+
+
+# --------------------------------------------------------------- arms ------
+def run_reference(a):
+    """The oracle on the host cores: each step is a bounded sample."""
+    from oracle import oracle as orc
+    world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    A, Bt = workloads.make_pair("spread", a.m, a.n, a.k, seed=0, phi=a.phi)
+    per_step = max(2.0, 120.0 / max(1, a.steps + a.warmup))
+    ent, dt, _, rc = oracle_sample(A, Bt, a, per_step)
+    for _ in range(a.warmup):
+        oracle_sample(A, Bt, a, per_step, rc)
+    times = []
+    for _ in range(a.steps):
+        e, t, _, _ = oracle_sample(A, Bt, a, per_step, rc)
+        times.append(t)
+    tot = sum(times)
+    value = 2.0 * a.k * ent * a.steps / tot / 1e12
+    sample = f"{len(rc[0])} rows x {len(rc[1])} columns of C (full k) per step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * tot / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config(a),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(a):
+    import torch
+
+    import rns_emulated_fp64_gb300 as os2
+    world, rank, local = dist_setup(a)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    m, n, k, N = a.m, a.n, a.k, a.num_moduli
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=rank, phi=a.phi)
+    Ad = torch.from_numpy(A).to(dev)
+    Bd = torch.from_numpy(Bt).to(dev)
+    Cd = torch.empty((m, n), dtype=torch.float64, device=dev)
+    ws = os2.alloc_workspace(os2.workspace_size(m, n, k, N, a.mode), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        os2.gemm(Ad, Bd, N, a.mode, out=Cd, workspace=ws, stream=stream)
+
+    for _ in range(a.warmup):
+        step()
+    st = os2.get_status(stream)
+    if st:
+        raise RuntimeError(f"device status after warm-up: {os2.status_string(st)}")
+
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    if not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    clocks = ClockSampler(uuid)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    os2.profile_start()
+    ev0.record(stream)
+    for _ in range(a.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    prof = os2.profile_stop()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    st = os2.get_status(stream)
+    if st:
+        raise RuntimeError(f"device status after timed steps: {os2.status_string(st)}")
+    ms_max = max_over_ranks(world, ms)
+    flop = 2.0 * m * n * k
+    value = world * flop * a.steps / (ms_max / 1e3) / 1e12
+
+    peaks, src = measured_peaks()
+    kern = {}
+    for name, (tot, cnt) in prof.items():
+        kern[name] = {"launches": cnt, "avg_ms": tot / max(cnt, 1), "share": None}
+    total_k = sum(v["avg_ms"] * v["launches"] for v in kern.values())
+    for v in kern.values():
+        v["share"] = v["avg_ms"] * v["launches"] / total_k if total_k else None
+    # algorithmic work per launch
+    kp = (k + 63) // 64 * 64
+    algo = {
+        "scale_residue_A": ("GB/s", 8.0 * m * k + 2.0 * N * m * kp),
+        "scale_residue_B": ("GB/s", 8.0 * n * k + 2.0 * N * n * kp),
+        "gemm_modp": ("TFLOP/s", 2.0 * N * m * n * k),
+        "crt_unscale": ("GB/s", 1.0 * N * m * n + 8.0 * m * n + 4.0 * (m + n)),
+    }
+    for name, v in kern.items():
+        if name in algo:
+            unit, work = algo[name]
+            secs = v["avg_ms"] / 1e3
+            if unit == "GB/s":
+                v["achieved"] = work / secs / 1e9
+                v["unit"] = "GB/s"
+                v["frac_of_hbm"] = v["achieved"] / peaks["hbm_gbs"]
+            else:
+                v["achieved"] = work / secs / 1e12
+                v["unit"] = "TFLOP/s"
+    g = kern.get("gemm_modp")
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    roofline = None
+    if g:
+        roofline = {"bound": "tensor", "kernel": "gemm_modp (tcgen05.mma kind::f16, FP16-held residues)",
+                    "achieved": g["achieved"], "peak": peak_t, "unit": "TFLOP/s",
+                    "frac": g["achieved"] / peak_t, "traffic": kernel_traffic("gemm_modp"),
+                    "peak_source": f"{src} bf16 dense sustained (FP16 rate = BF16 rate)",
+                    "work_per_launch": f"N*2mnk = {2.0 * N * m * n * k:.4g} flop"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config(a), "clocks": clk,
+            "gpu_launches": os2.launch_count(m, n, k, N, a.mode) * a.steps,
+            "roofline": roofline, "kernels": kern}
+
+    # e2e through the host entry point
+    if not a.no_e2e:
+        Ah = torch.from_numpy(A).pin_memory()
+        Bh = torch.from_numpy(Bt).pin_memory()
+        Ch = torch.empty((m, n), dtype=torch.float64).pin_memory()
+        wsh = os2.alloc_workspace(os2.host_workspace_size(m, n, k, N, a.mode), dev)
+        del ws
+        torch.cuda.empty_cache()
+        for _ in range(2):
+            os2.gemm_host(Ah, Bh, Ch, N, a.mode, workspace=wsh, stream=stream)
+        torch.cuda.synchronize(dev)
+        ke = max(3, min(a.steps, 10))
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(ke):
+            os2.gemm_host(Ah, Bh, Ch, N, a.mode, workspace=wsh, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ems = max_over_ranks(world, e0.elapsed_time(e1))
+        line["e2e"] = {"value": world * flop * ke / (ems / 1e3) / 1e12, "unit": UNIT,
+                       "h2d_bytes_per_step": 8 * (m * k + n * k), "d2h_bytes_per_step": 8 * m * n,
+                       "steps": ke, "ms_per_step": ems / ke}
+        assert torch.equal(Ch, Cd.cpu()), "host entry point result differs from device entry point"
+        del wsh
+
+    # CPU oracle baseline + bit-exact check of the benchmarked result on the same sample
+    if rank == 0 and not a.no_cpu_baseline:
+        from oracle import oracle as orc
+        ent, dt, ref, (rows, cols) = oracle_sample(A, Bt, a, a.cpu_seconds)
+        got = Cd.cpu().numpy()[np.ix_(rows, cols)]
+        same = bool(np.array_equal(got.view(np.uint64), ref.C.view(np.uint64)))
+        line["cpu_baseline"] = {"value": 2.0 * k * ent / dt / 1e12, "unit": UNIT,
+                                "cores": orc.num_threads(), "kind": "oracle",
+                                "sample": f"{len(rows)} rows x {len(cols)} columns of C (full k), "
+                                          f"{dt:.1f} s",
+                                "gpu_result_bit_exact_on_sample": same}
+        if not same:
+            line["parity_error"] = int(np.count_nonzero(got != ref.C))
+
+    # context: native cuBLAS DGEMM rate and accuracy against the exact product
+    if rank == 0 and not a.no_context:
+        Bk = Bd.t()
+        torch.matmul(Ad, Bk)
+        torch.cuda.synchronize(dev)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        Cn = torch.matmul(Ad, Bk)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        nat_ms = t0.elapsed_time(t1)
+        rr, cc = workloads.sample_grid(m, n, 6, seed=2)
+        Ce = Cd.cpu().numpy()
+        Cnn = Cn.cpu().numpy()
+        e_emu = e_nat = 0.0
+        for i in rr:
+            for j in cc:
+                ex = exact_dot(A[i], Bt[j])
+                scale = float(np.abs(A[i]) @ np.abs(Bt[j]))
+                e_emu = max(e_emu, abs(Ce[i, j] - ex) / scale)
+                e_nat = max(e_nat, abs(Cnn[i, j] - ex) / scale)
+        line["context"] = {"native_dgemm_tflops": flop / (nat_ms / 1e3) / 1e12,
+                           "native_dgemm": "torch.matmul float64 (cuBLAS DGEMM)",
+                           "max_err_over_absprod_emulated": e_emu,
+                           "max_err_over_absprod_native": e_nat,
+                           "error_sample": f"{len(rr)}x{len(cc)} entries vs exact (fsum)"}
+        del Cn
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+
+
+if __name__ == "__main__":
+    main()

@@ -149,6 +149,18 @@ const char *os2_status_string(int status);
  * accounting); 0 on bad args. */
 int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode);
 
+/* Per-kernel timing of os2_gemm / os2_gemm_host (a measurement aid; the pages
+ * define no such call).  os2_profile_start() enables it: every kernel those
+ * calls enqueue is then bracketed by two CUDA events on the caller's stream.
+ * os2_profile_stop() disables it, waits for the recorded events, and writes
+ * up to max_kernels aggregated entries: names[i*32..] (NUL-terminated kernel
+ * role: scale_residue_A, scale_residue_B, gemm_bound, gemm_modp, crt_unscale),
+ * total_ms[i] and launches[i].  Returns the entry count, or -1 if an event
+ * failed.  Any output pointer may be NULL.  Process-wide, not thread-safe
+ * against concurrent os2_gemm calls on other threads. */
+os2_status os2_profile_start(void);
+int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ KP_ALIGN, CRES_ALIGN = 64, 16
 EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gemm_host",
            "os2_scale", "os2_residues", "os2_gemm_residues", "os2_crt", "os2_moduli",
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
-           "os2_gemm_launch_count")
+           "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop")
 
 _lib = None
 _lock = threading.Lock()
@@ -80,6 +80,10 @@ def load(build_if_missing: bool = True):
         L.os2_status_string.restype = ct.c_char_p
         L.os2_gemm_launch_count.argtypes = [i, i, i, i, i]
         L.os2_gemm_launch_count.restype = i
+        L.os2_profile_start.argtypes = []
+        L.os2_profile_start.restype = i
+        L.os2_profile_stop.argtypes = [i, vp, vp, vp]
+        L.os2_profile_stop.restype = i
         _lib = L
         return L
 
@@ -257,3 +261,20 @@ def crt(cres, n, e, f, want_X=False, stream=None):
                         _stream(stream))
     _check(st, "os2_crt")
     return (C, X) if want_X else C
+
+
+def profile_start():
+    """Start per-kernel CUDA-event timing of os2_gemm launches."""
+    _check(load().os2_profile_start(), "os2_profile_start")
+
+
+def profile_stop() -> dict:
+    """Stop timing; returns {kernel role: (total_ms, launches)}."""
+    names = ct.create_string_buffer(32 * 16)
+    tot = (ct.c_double * 16)()
+    cnt = (ct.c_int * 16)()
+    n = load().os2_profile_stop(16, names, tot, cnt)
+    if n < 0:
+        raise Os2Error(ERR_CUDA, "os2_profile_stop")
+    raw = names.raw
+    return {raw[32 * i:32 * i + 32].split(b"\0")[0].decode(): (tot[i], cnt[i]) for i in range(n)}

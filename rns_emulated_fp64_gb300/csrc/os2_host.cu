@@ -6,6 +6,8 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "os2_internal.cuh"
 
@@ -144,6 +146,33 @@ void build_tables(int N, Os2Tables *t) {
 
 std::atomic<int> g_variant{OS2_GEMM_TC};
 
+// Optional per-kernel timing: CUDA events recorded on the launching stream
+// around every kernel that os2_gemm enqueues (no synchronisation added).
+struct ProfRec {
+  const char *name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof;
+std::atomic<bool> g_prof_on{false};
+
+struct ProfScope {
+  const char *name;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  ProfScope(const char *n, cudaStream_t st) : name(n), s(st) {
+    if (g_prof_on.load() && cudaEventCreate(&a) == cudaSuccess) cudaEventRecord(a, s);
+  }
+  ~ProfScope() {
+    cudaEvent_t b = nullptr;
+    if (a && cudaEventCreate(&b) == cudaSuccess) {
+      cudaEventRecord(b, s);
+      std::lock_guard<std::mutex> g(g_prof_mu);
+      g_prof.push_back({name, a, b});
+    }
+  }
+};
+
 }  // namespace
 
 const Os2Tables *os2_tables(int N) {
@@ -236,10 +265,16 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
   cudaError_t err;
   if (mode == OS2_MODE_FAST) {
     // steps 1 + 2 fused: exponents from the revised bound, then residue planes
-    if ((err = launch_scale_residue(SM_FAST_FUSED, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
-      return cuda_status(err);
-    if ((err = launch_scale_residue(SM_FAST_FUSED, B, ldb, n, k, L.kp, f, nullptr, pb, t, status, s)))
-      return cuda_status(err);
+    {
+      ProfScope ps("scale_residue_A", s);
+      if ((err = launch_scale_residue(SM_FAST_FUSED, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
+        return cuda_status(err);
+    }
+    {
+      ProfScope ps("scale_residue_B", s);
+      if ((err = launch_scale_residue(SM_FAST_FUSED, B, ldb, n, k, L.kp, f, nullptr, pb, t, status, s)))
+        return cuda_status(err);
+    }
   } else {
     // step 1, accurate: magnitude planes (aliasing the residue planes), one
     // exact bound product with fused row/column maxima, exponents; then step 2
@@ -251,8 +286,11 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
       return cuda_status(err);
     if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
     if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
-    if ((err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
-      return cuda_status(err);
+    {
+      ProfScope ps("gemm_bound", s);
+      if ((err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
+        return cuda_status(err);
+    }
     if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
     if ((err = launch_accu_exponents(K, EB, n, f, t, s))) return cuda_status(err);
     if ((err = launch_scale_residue(SM_RESIDUES, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
@@ -261,13 +299,17 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
       return cuda_status(err);
   }
   // step 3
-  if (g_variant.load() == OS2_GEMM_SIMT)
-    err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
-  else
-    err = launch_gemm_tc(0, m, n, L.kp, pa, pb, N, cres, L.ldcres, nullptr, nullptr, 14, t,
-                         status, s);
-  if (err) return cuda_status(err);
+  {
+    ProfScope ps("gemm_modp", s);
+    if (g_variant.load() == OS2_GEMM_SIMT)
+      err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
+    else
+      err = launch_gemm_tc(0, m, n, L.kp, pa, pb, N, cres, L.ldcres, nullptr, nullptr, 14, t,
+                           status, s);
+    if (err) return cuda_status(err);
+  }
   // steps 4 + 5
+  ProfScope ps("crt_unscale", s);
   return cuda_status(launch_crt(m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
 }
 
@@ -473,6 +515,54 @@ const char *os2_status_string(int status) {
     case OS2_ERR_CUDA: return "CUDA error";
   }
   return "unknown status";
+}
+
+os2_status os2_profile_start(void) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto &r : g_prof) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof.clear();
+  g_prof_on.store(true);
+  return OS2_OK;
+}
+
+int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launches) {
+  g_prof_on.store(false);
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  std::vector<std::string> keys;
+  std::vector<double> tot;
+  std::vector<int> cnt;
+  int bad = 0;
+  for (auto &r : g_prof) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+      bad = 1;
+    size_t i = 0;
+    while (i < keys.size() && keys[i] != r.name) i++;
+    if (i == keys.size()) {
+      keys.push_back(r.name);
+      tot.push_back(0.0);
+      cnt.push_back(0);
+    }
+    tot[i] += ms;
+    cnt[i] += 1;
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  g_prof.clear();
+  if (bad) return -1;
+  int n = 0;
+  for (size_t i = 0; i < keys.size() && n < max_kernels; i++, n++) {
+    if (names) {
+      strncpy(names + 32 * n, keys[i].c_str(), 31);
+      names[32 * n + 31] = 0;
+    }
+    if (total_ms) total_ms[n] = tot[i];
+    if (launches) launches[n] = cnt[i];
+  }
+  return n;
 }
 
 int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
