@@ -161,6 +161,33 @@ int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode);
 os2_status os2_profile_start(void);
 int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launches);
 
+/* os2_gemm without a caller-supplied workspace, for callers that cannot
+ * allocate device memory where they call it: a host library or plugin whose
+ * device memory is planned and owned by another allocator (an inference
+ * runtime's arena, a framework's caching allocator) and which has no
+ * workspace to hand over, or a latency-critical loop that must not call
+ * cudaMalloc/cudaFree because those calls can synchronise the whole device.
+ * The pages have no counterpart of this call; it only changes where the
+ * scratch lives.
+ *
+ * The scratch is one static device array of OS2_NOALLOC_SCRATCH_BYTES
+ * (128 MiB) inside libos2; every GPU that loads the library holds it until
+ * the process exits.  Problems whose os2_workspace_size exceeds it are
+ * rejected with OS2_ERR_WORKSPACE before anything is enqueued (for example
+ * m = n = k = 1024 fits for every num_moduli <= 20; at 2048^3 only
+ * num_moduli <= 6 fits).
+ * The first call on a device looks up the array's device address with that
+ * device current (make that first call before any stream capture); later
+ * calls reuse it.  Nothing here calls cudaMalloc, cudaFree or an allocating
+ * library routine.  Every call uses the same array and the array keeps the
+ * previous call's contents (each call clears what it needs zeroed), so calls
+ * that overlap on the GPU -- on different streams or from different threads
+ * -- race and corrupt each other's results: serialise them.  Arguments,
+ * layouts, errors and results are those of os2_gemm. */
+#define OS2_NOALLOC_SCRATCH_BYTES (128u << 20)
+os2_status os2_gemm_noalloc(int m, int n, int k, const double *A, int lda, const double *B,
+                            int ldb, double *C, int ldc, int num_moduli, int mode, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

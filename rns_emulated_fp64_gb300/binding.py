@@ -25,7 +25,8 @@ KP_ALIGN, CRES_ALIGN = 64, 16
 EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gemm_host",
            "os2_scale", "os2_residues", "os2_gemm_residues", "os2_crt", "os2_moduli",
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
-           "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop")
+           "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
+           "os2_gemm_noalloc")
 
 _lib = None
 _lock = threading.Lock()
@@ -84,6 +85,8 @@ def load(build_if_missing: bool = True):
         L.os2_profile_start.restype = i
         L.os2_profile_stop.argtypes = [i, vp, vp, vp]
         L.os2_profile_stop.restype = i
+        L.os2_gemm_noalloc.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp]
+        L.os2_gemm_noalloc.restype = i
         _lib = L
         return L
 
@@ -278,3 +281,27 @@ def profile_stop() -> dict:
         raise Os2Error(ERR_CUDA, "os2_profile_stop")
     raw = names.raw
     return {raw[32 * i:32 * i + 32].split(b"\0")[0].decode(): (tot[i], cnt[i]) for i in range(n)}
+
+
+NOALLOC_SCRATCH_BYTES = 128 << 20
+
+
+def gemm_noalloc(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 14, mode="fast", out=None,
+                 stream=None) -> torch.Tensor:
+    """C = A @ Bt.T like ``gemm``, for callers that cannot allocate device
+    memory at the call: the scratch is a fixed 128 MiB array inside libos2
+    (shared by every call; serialise calls that could overlap on the GPU).
+    ``out`` must be given by such callers; the default allocates it here."""
+    A, lda = _kmat(A, "A")
+    Bt, ldb = _kmat(Bt, "Bt")
+    m, k = A.shape
+    n = Bt.shape[0]
+    if Bt.shape[1] != k:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float64, device=A.device)
+    ldc = max(out.stride(0), max(n, 1))
+    st = load().os2_gemm_noalloc(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, _ptr(out), ldc,
+                                 num_moduli, _mode(mode), _stream(stream))
+    _check(st, "os2_gemm_noalloc")
+    return out

@@ -572,3 +572,46 @@ int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// os2_gemm_noalloc: os2_gemm for callers that cannot allocate device memory.
+// Its scratch lives in one file-scope device array of fixed size; every GPU
+// that loads this library holds that array until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_os2_noalloc_scratch[OS2_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.  In host code the array's name is
+// only a host-side stand-in, so kernels must be given this address.
+void *noalloc_scratch() {
+  static std::mutex mu;
+  static void *ptrs[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_os2_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+
+extern "C" os2_status os2_gemm_noalloc(int m, int n, int k, const double *A, int lda,
+                                       const double *B, int ldb, double *C, int ldc,
+                                       int num_moduli, int mode, void *stream) {
+  os2_status st = check_gemm_args(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode);
+  if (st) return st;
+  Layout L;
+  make_layout(m, n, k, num_moduli, mode, &L);
+  if (m == 0 || n == 0) return OS2_OK;
+  if (L.total > (size_t)OS2_NOALLOC_SCRATCH_BYTES) return OS2_ERR_WORKSPACE;
+  void *ws = noalloc_scratch();
+  if (!ws) return OS2_ERR_CUDA;
+  return run_gemm(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, ws, L,
+                  static_cast<cudaStream_t>(stream));
+}
