@@ -308,8 +308,10 @@ def run_ours(a):
     # algorithmic work per launch
     kp = (k + 63) // 64 * 64
     algo = {
-        "scale_residue_A": ("GB/s", 8.0 * m * k + 2.0 * N * m * kp),
-        "scale_residue_B": ("GB/s", 8.0 * n * k + 2.0 * N * n * kp),
+        "scale": ("GB/s", 8.0 * (m + n) * k),
+        "scale_bars": ("GB/s", 8.0 * (m + n) * k + 2.0 * (m + n) * kp),
+        "residues": ("GB/s", 8.0 * (m + n) * k + 2.0 * N * (m + n) * kp),
+        "gemm_bound": ("TFLOP/s", 2.0 * m * n * k),
         "gemm_modp": ("TFLOP/s", 2.0 * N * m * n * k),
         "crt_unscale": ("GB/s", 1.0 * N * m * n + 8.0 * m * n + 4.0 * (m + n)),
     }

@@ -15,9 +15,18 @@
 // [-floor(p/2), ceil(p/2) - 1], which always fit int8 and are stored as FP16
 // (exact for |r| <= 2048) for the tensor-core products of step 3.
 //
-// Layout: one CTA of 256 threads per row; the row is read up to three times
-// (exponent, sum of squares, residues), the re-reads hit L1/L2.  Every
-// residue plane row is written with 16-byte stores, 8 values per thread.
+// Two kernels, each launched once for both operands (A's rows, then B's
+// columns):
+//   k_row_scale  one CTA per row: exponent bound (pass 1), then either the
+//                fast-mode sum of squares and e_i, or the accurate-mode
+//                7-bit magnitude plane (pass 2 re-reads the row from L1/L2).
+//   k_residues   element-parallel: every thread turns 8 consecutive entries
+//                into 8 residues per modulus and writes one 16-byte vector to
+//                each plane.  Residues of the odd moduli use FP32 arithmetic
+//                only: the integer is split into 12-bit words w_t and
+//                x = sum_t w_t (2^(12t) mod p) is exact below 2^23, so one
+//                fused multiply-add rounds x / p to the nearest integer
+//                exactly; mod 256 is the integer's low byte.
 #include <cuda_fp16.h>
 #include <limits.h>
 
@@ -117,8 +126,88 @@ __device__ __forceinline__ void set_status(int *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
-// 12-bit words of trunc(mant * 2^sh) (< 2^84), negated for negative inputs.
-__device__ __forceinline__ void int_words(const Dec &d, int sh, float (&w)[7]) {
+struct RowSet {
+  const double *X;
+  long ldx;
+  int rows;
+  int32_t *e;       // exponents (out for scale, in for residues)
+  int32_t *E;       // accurate mode: exponent bounds (out)
+  __half *planes;   // residue planes [N][rows][kp] or the magnitude plane [rows][kp]
+};
+
+// ------------------------------------------------------------- row scale ---
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+    k_row_scale(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
+  __shared__ int s_int[32];
+  __shared__ unsigned long long s_u64[32];
+  const bool isA = (int)blockIdx.x < a.rows;
+  const RowSet &rs = isA ? a : b;
+  const int row = isA ? (int)blockIdx.x : (int)blockIdx.x - a.rows;
+  const double *x = rs.X + (size_t)row * rs.ldx;
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+
+  // pass 1: exponent bound and finiteness
+  int emax = INT_MIN, bad = 0;
+  if (vec) {
+    for (int h = 2 * threadIdx.x; h < k; h += 2 * kThreads) {
+      if (h + 1 < k) {
+        const double2 v = __ldg(reinterpret_cast<const double2 *>(x + h));
+        const Dec d0 = decode(v.x), d1 = decode(v.y);
+        bad |= d0.nonfinite | d1.nonfinite;
+        emax = max(emax, max(exp_bound(d0), exp_bound(d1)));
+      } else {
+        const Dec d0 = decode(__ldg(x + h));
+        bad |= d0.nonfinite;
+        emax = max(emax, exp_bound(d0));
+      }
+    }
+  } else {
+    for (int h = threadIdx.x; h < k; h += kThreads) {
+      const Dec d = decode(__ldg(x + h));
+      bad |= d.nonfinite;
+      emax = max(emax, exp_bound(d));
+    }
+  }
+  emax = block_max(emax, s_int);
+  bad = block_max(bad, s_int);
+  if (bad && threadIdx.x == 0) set_status(status, OS2_ERR_NONFINITE);
+  const bool nonzero = emax != INT_MIN;
+  const int E = nonzero ? emax : 0;
+
+  if (MODE == SM_BARS) {
+    // accurate mode: E_i and Abar_ih = ceil(|a_ih| 2^(6 - E_i)) in [0, 64]
+    if (threadIdx.x == 0) rs.E[row] = E;
+    __half *dst = rs.planes + (size_t)row * kp;
+    for (int ch = threadIdx.x; ch < kp / 8; ch += kThreads) {
+      const int h0 = ch * 8;
+      __align__(16) __half v[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int h = h0 + u;
+        const Dec d = decode(h < k ? __ldg(x + h) : 0.0);
+        v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
+      }
+      *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
+    }
+    return;
+  }
+
+  // pass 2 (fast mode): exact sum of squares of the 23-bit upper roundings
+  unsigned long long Q = 0;
+  for (int h = threadIdx.x; h < k; h += kThreads) {
+    const Dec d = decode(__ldg(x + h));
+    const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
+    Q += q * q;
+  }
+  Q = block_sum(Q, s_u64);
+  if (threadIdx.x == 0) rs.e[row] = (nonzero && !bad && Q) ? largest_g(Q, c) + 23 - E : 0;
+}
+
+// --------------------------------------------------------------- residues --
+// 12-bit words of trunc(mant * 2^sh) (< 2^84) as floats carrying the sign.
+template <int NW>
+__device__ __forceinline__ void int_words(const Dec &d, int sh, float (&w)[7], uint32_t &lowbyte) {
   uint64_t lo, hi;
   if (d.mant == 0) {
     lo = hi = 0;
@@ -127,116 +216,118 @@ __device__ __forceinline__ void int_words(const Dec &d, int sh, float (&w)[7]) {
     else if (sh < 64) { lo = d.mant << sh; hi = d.mant >> (64 - sh); }
     else { lo = 0; hi = d.mant << (sh - 64); }
   } else {
-    int r = -sh;
+    const int r = -sh;
     lo = r >= 64 ? 0 : (d.mant >> r);
     hi = 0;
   }
+  // low byte of the signed integer (two's complement): its residue mod 256
+  lowbyte = (uint32_t)(d.neg ? (0ull - lo) : lo) & 0xFFu;
+  // +-(2^23 + u) from the bit pattern, then -+2^23: exact signed word as float
+  const uint32_t base = d.neg ? 0xCB000000u : 0x4B000000u;
+  const float off = d.neg ? 8388608.0f : -8388608.0f;
   uint32_t u[7];
   u[0] = (uint32_t)(lo & 0xFFF);
   u[1] = (uint32_t)((lo >> 12) & 0xFFF);
   u[2] = (uint32_t)((lo >> 24) & 0xFFF);
   u[3] = (uint32_t)((lo >> 36) & 0xFFF);
   u[4] = (uint32_t)((lo >> 48) & 0xFFF);
-  u[5] = (uint32_t)(((lo >> 60) | (hi << 4)) & 0xFFF);
-  u[6] = (uint32_t)((hi >> 8) & 0xFFF);
+  if (NW > 5) {
+    u[5] = (uint32_t)(((lo >> 60) | (hi << 4)) & 0xFFF);
+    u[6] = (uint32_t)((hi >> 8) & 0xFFF);
+  }
 #pragma unroll
-  for (int t = 0; t < 7; t++) w[t] = d.neg ? -(float)u[t] : (float)u[t];
+  for (int t = 0; t < NW; t++) w[t] = __uint_as_float(base | u[t]) + off;
 }
 
-// Symmetric residue of sum_t w_t 2^(12t) modulo p_l.  Every partial sum is an
-// integer below 7 * 4095 * 128 < 2^24, so the FP32 chain is exact; the
-// rounded quotient is off by at most one, fixed by one step each way.
-__device__ __forceinline__ float residue(const float (&w)[7], const ResConsts &c, int l) {
+// Residue of sum_t w_t 2^(12t) mod odd p_l, canonical.  |x| <= 7*4095*127 <
+// 2^23, so x * fl(1/p) is within 1/(2p) of x/p, which is at least 1/(2p) from
+// any half-integer: the FMA-with-magic-constant rounding gives round(x/p).
+template <int NW>
+__device__ __forceinline__ float residue_odd(const float (&w)[7], const ResConsts &c, int l) {
   float x = w[0] * c.w12[l][0];
 #pragma unroll
-  for (int t = 1; t < 7; t++) x = fmaf(w[t], c.w12[l][t], x);
-  float q = rintf(x * c.invp[l]);
-  float r = fmaf(-c.p[l], q, x);
-  r = r > c.hi[l] ? r - c.p[l] : r;
-  r = r < c.lo[l] ? r + c.p[l] : r;
-  return r;
+  for (int t = 1; t < NW; t++) x = fmaf(w[t], c.w12[l][t], x);
+  const float q = fmaf(x, c.invp[l], 12582912.0f) - 12582912.0f;  // 1.5 * 2^23
+  return fmaf(-c.p[l], q, x);
 }
 
-template <int N, int MODE>
-__global__ void __launch_bounds__(kThreads)
-    k_scale_residue(const double *__restrict__ X, long ldx, int rows, int k, int kp,
-                    int32_t *__restrict__ e, int32_t *__restrict__ Eout,
-                    __half *__restrict__ planes, const ResConsts c, int *status) {
-  __shared__ int s_int[32];
-  __shared__ unsigned long long s_u64[32];
-  __shared__ int s_e;
-  const int row = blockIdx.x;
-  const double *x = X + (size_t)row * ldx;
-  int ee = 0;
+__device__ __forceinline__ float byte_residue(uint32_t b) {
+  return (float)((int)(b ^ 0x80u) - 128);  // [-128, 127]
+}
 
-  if (MODE != SM_RESIDUES) {
-    int emax = INT_MIN, bad = 0;
-    for (int h = threadIdx.x; h < k; h += kThreads) {
-      Dec d = decode(__ldg(x + h));
-      bad |= d.nonfinite;
-      emax = max(emax, exp_bound(d));
-    }
-    emax = block_max(emax, s_int);
-    bad = block_max(bad, s_int);
-    if (bad && threadIdx.x == 0) set_status(status, OS2_ERR_NONFINITE);
-    const bool nonzero = emax != INT_MIN;
-    const int E = nonzero ? emax : 0;
+template <int N, int NW>
+__device__ __forceinline__ void emit(const float (&w)[8][7], const uint32_t (&lb)[8],
+                                     const ResConsts &c, __half *dst, size_t pstride) {
+  {
+    __align__(16) __half2 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+      v[u] = __floats2half2_rn(byte_residue(lb[2 * u]), byte_residue(lb[2 * u + 1]));
+    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(v);
+  }
+#pragma unroll
+  for (int l = 1; l < N; l++) {
+    __align__(16) __half2 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+      v[u] = __floats2half2_rn(residue_odd<NW>(w[2 * u], c, l),
+                               residue_odd<NW>(w[2 * u + 1], c, l));
+    *reinterpret_cast<uint4 *>(dst + l * pstride) = *reinterpret_cast<uint4 *>(v);
+  }
+}
 
-    if (MODE == SM_BARS) {
-      // accurate mode: E_i and Abar_ih = ceil(|a_ih| 2^(6 - E_i)) in [0, 64]
-      if (threadIdx.x == 0) Eout[row] = E;
-      __half *dst = planes + (size_t)row * kp;
-      for (int ch = threadIdx.x; ch < kp / 8; ch += kThreads) {
-        int h0 = ch * 8;
-        __align__(16) __half v[8];
+template <int N>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_residues(const RowSet a, const RowSet b, int k, int kp, const ResConsts c) {
+  const int cpr = kp / 8;  // 8-entry chunks per row
+  const int total_rows = a.rows + b.rows;
+  for (int rr = blockIdx.y; rr < total_rows; rr += gridDim.y) {
+    const bool isA = rr < a.rows;
+    const RowSet &rs = isA ? a : b;
+    const int row = isA ? rr : rr - a.rows;
+    const double *x = rs.X + (size_t)row * rs.ldx;
+    const int ee = __ldg(rs.e + row);
+    const size_t pstride = (size_t)rs.rows * kp;
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    for (int ch = blockIdx.x * kThreads + threadIdx.x; ch < cpr; ch += gridDim.x * kThreads) {
+      const int h0 = ch * 8;
+      double v[8];
+      if (vec && h0 + 8 <= k) {
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+          const double2 t = __ldg(reinterpret_cast<const double2 *>(x + h0) + u);
+          v[2 * u] = t.x;
+          v[2 * u + 1] = t.y;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; u++) v[u] = h0 + u < k ? __ldg(x + h0 + u) : 0.0;
+      }
+      // bit length bound of the 8 integers (row exponent + element exponent)
+      int top = INT_MIN;
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const uint64_t bits = (uint64_t)__double_as_longlong(v[u]);
+        if (bits << 1) top = max(top, max((int)((bits >> 52) & 0x7FF), 1) - 1022 + ee);
+      }
+      float w[8][7];
+      uint32_t lb[8];
+      __half *dst = rs.planes + (size_t)row * kp + h0;
+      if (top <= 60) {
 #pragma unroll
         for (int u = 0; u < 8; u++) {
-          int h = h0 + u;
-          Dec d = decode(h < k ? __ldg(x + h) : 0.0);
-          v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
+          const Dec d = decode(v[u]);
+          int_words<5>(d, d.ex2 + ee, w[u], lb[u]);
         }
-        *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
+        emit<N, 5>(w, lb, c, dst, pstride);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+          const Dec d = decode(v[u]);
+          int_words<7>(d, d.ex2 + ee, w[u], lb[u]);
+        }
+        emit<N, 7>(w, lb, c, dst, pstride);
       }
-      return;
-    }
-
-    unsigned long long Q = 0;
-    for (int h = threadIdx.x; h < k; h += kThreads) {
-      Dec d = decode(__ldg(x + h));
-      unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
-      Q += q * q;
-    }
-    Q = block_sum(Q, s_u64);
-    if (threadIdx.x == 0) {
-      int v = (nonzero && !bad && Q) ? largest_g(Q, c) + 23 - E : 0;
-      e[row] = v;
-      s_e = v;
-    }
-    __syncthreads();
-    ee = s_e;
-    if (MODE == SM_FAST_SCALE) return;
-  } else {
-    ee = e[row];
-  }
-
-  // residue planes: plane l, row `row`, columns [h0, h0 + 8) per thread
-  for (int ch = threadIdx.x; ch < kp / 8; ch += kThreads) {
-    const int h0 = ch * 8;
-    float w[8][7];
-#pragma unroll
-    for (int u = 0; u < 8; u++) {
-      int h = h0 + u;
-      Dec d = decode(h < k ? __ldg(x + h) : 0.0);
-      int_words(d, d.ex2 + ee, w[u]);
-    }
-#pragma unroll
-    for (int l = 0; l < N; l++) {
-      __align__(16) __half2 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; u++)
-        v[u] = __floats2half2_rn(residue(w[2 * u], c, l), residue(w[2 * u + 1], c, l));
-      *reinterpret_cast<uint4 *>(planes + ((size_t)l * rows + row) * kp + h0) =
-          *reinterpret_cast<uint4 *>(v);
     }
   }
 }
@@ -249,16 +340,39 @@ __global__ void k_accu_exponents(const int32_t *__restrict__ bound, const int32_
   e[i] = R > 0 ? largest_g((uint64_t)R, c) + 6 - E[i] : -E[i];
 }
 
-template <int MODE>
-cudaError_t dispatch(int N, dim3 grid, cudaStream_t s, const double *X, long ldx, int rows, int k,
-                     int kp, int32_t *e, int32_t *E, __half *planes, const ResConsts &c,
-                     int *status) {
-#define OS2_CASE(NN)                                                                          \
-  case NN:                                                                                    \
-    k_scale_residue<NN, MODE><<<grid, kThreads, 0, s>>>(X, ldx, rows, k, kp, e, E, planes, c, \
-                                                        status);                              \
+}  // namespace
+
+cudaError_t launch_row_scale(int mode, const double *XA, long lda, int rowsA, int32_t *eA,
+                             int32_t *EA, void *barsA, const double *XB, long ldb, int rowsB,
+                             int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
+                             const Os2Tables *t, int *status, cudaStream_t s) {
+  if (rowsA + rowsB <= 0) return cudaSuccess;
+  RowSet a{XA, lda, rowsA, eA, EA, reinterpret_cast<__half *>(barsA)};
+  RowSet b{XB, ldb, rowsB, eB, EB, reinterpret_cast<__half *>(barsB)};
+  dim3 grid(rowsA + rowsB);
+  if (mode == SM_BARS)
+    k_row_scale<SM_BARS><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+  else
+    k_row_scale<SM_FAST_SCALE><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residues(const double *XA, long lda, int rowsA, const int32_t *eA,
+                            void *planesA, const double *XB, long ldb, int rowsB,
+                            const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
+                            cudaStream_t s) {
+  if (rowsA + rowsB <= 0 || kp <= 0) return cudaSuccess;
+  RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA)};
+  RowSet b{XB, ldb, rowsB, const_cast<int32_t *>(eB), nullptr, reinterpret_cast<__half *>(planesB)};
+  const int cpr = kp / 8;
+  const int bx = (cpr + kThreads - 1) / kThreads;
+  const int rows = rowsA + rowsB;
+  dim3 grid(bx, rows < 65535 ? rows : 65535);
+#define OS2_CASE(NN)                                                         \
+  case NN:                                                                   \
+    k_residues<NN><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res);           \
     break;
-  switch (N) {
+  switch (t->N) {
     OS2_CASE(1) OS2_CASE(2) OS2_CASE(3) OS2_CASE(4) OS2_CASE(5) OS2_CASE(6) OS2_CASE(7)
     OS2_CASE(8) OS2_CASE(9) OS2_CASE(10) OS2_CASE(11) OS2_CASE(12) OS2_CASE(13) OS2_CASE(14)
     OS2_CASE(15) OS2_CASE(16) OS2_CASE(17) OS2_CASE(18) OS2_CASE(19) OS2_CASE(20)
@@ -266,31 +380,6 @@ cudaError_t dispatch(int N, dim3 grid, cudaStream_t s, const double *X, long ldx
   }
 #undef OS2_CASE
   return cudaGetLastError();
-}
-
-}  // namespace
-
-cudaError_t launch_scale_residue(int mode, const double *X, long ldx, int rows, int k, int kp,
-                                 int32_t *e, int32_t *E, void *planes, const Os2Tables *t,
-                                 int *status, cudaStream_t s) {
-  if (rows <= 0) return cudaSuccess;
-  dim3 grid(rows);
-  __half *pl = reinterpret_cast<__half *>(planes);
-  switch (mode) {
-    case SM_FAST_FUSED:
-      return dispatch<SM_FAST_FUSED>(t->N, grid, s, X, ldx, rows, k, kp, e, E, pl, t->res, status);
-    case SM_RESIDUES:
-      return dispatch<SM_RESIDUES>(t->N, grid, s, X, ldx, rows, k, kp, e, E, pl, t->res, status);
-    case SM_FAST_SCALE:
-      k_scale_residue<1, SM_FAST_SCALE>
-          <<<grid, kThreads, 0, s>>>(X, ldx, rows, k, kp, e, E, pl, t->res, status);
-      return cudaGetLastError();
-    case SM_BARS:
-      k_scale_residue<1, SM_BARS>
-          <<<grid, kThreads, 0, s>>>(X, ldx, rows, k, kp, e, E, pl, t->res, status);
-      return cudaGetLastError();
-  }
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,

@@ -264,26 +264,22 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
   int8_t *cres = at<int8_t>(ws, L.cres);
   cudaError_t err;
   if (mode == OS2_MODE_FAST) {
-    // steps 1 + 2 fused: exponents from the revised bound, then residue planes
-    {
-      ProfScope ps("scale_residue_A", s);
-      if ((err = launch_scale_residue(SM_FAST_FUSED, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
-        return cuda_status(err);
-    }
-    {
-      ProfScope ps("scale_residue_B", s);
-      if ((err = launch_scale_residue(SM_FAST_FUSED, B, ldb, n, k, L.kp, f, nullptr, pb, t, status, s)))
-        return cuda_status(err);
-    }
+    // step 1: exponents from the revised bound (A's rows and B's columns)
+    ProfScope ps("scale", s);
+    if ((err = launch_row_scale(SM_FAST_SCALE, A, lda, m, e, nullptr, nullptr, B, ldb, n, f,
+                                nullptr, nullptr, k, L.kp, t, status, s)))
+      return cuda_status(err);
   } else {
     // step 1, accurate: magnitude planes (aliasing the residue planes), one
-    // exact bound product with fused row/column maxima, exponents; then step 2
+    // exact bound product with fused row/column maxima, exponents
     int32_t *EA = at<int32_t>(ws, L.EA), *EB = at<int32_t>(ws, L.EB);
     int32_t *R = at<int32_t>(ws, L.R), *K = at<int32_t>(ws, L.K);
-    if ((err = launch_scale_residue(SM_BARS, A, lda, m, k, L.kp, nullptr, EA, pa, t, status, s)))
-      return cuda_status(err);
-    if ((err = launch_scale_residue(SM_BARS, B, ldb, n, k, L.kp, nullptr, EB, pb, t, status, s)))
-      return cuda_status(err);
+    {
+      ProfScope ps("scale_bars", s);
+      if ((err = launch_row_scale(SM_BARS, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB, pb,
+                                  k, L.kp, t, status, s)))
+        return cuda_status(err);
+    }
     if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
     if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
     {
@@ -293,9 +289,11 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
     }
     if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
     if ((err = launch_accu_exponents(K, EB, n, f, t, s))) return cuda_status(err);
-    if ((err = launch_scale_residue(SM_RESIDUES, A, lda, m, k, L.kp, e, nullptr, pa, t, status, s)))
-      return cuda_status(err);
-    if ((err = launch_scale_residue(SM_RESIDUES, B, ldb, n, k, L.kp, f, nullptr, pb, t, status, s)))
+  }
+  // step 2: residue planes of A and B
+  {
+    ProfScope ps("residues", s);
+    if ((err = launch_residues(A, lda, m, e, pa, B, ldb, n, f, pb, k, L.kp, t, s)))
       return cuda_status(err);
   }
   // step 3
@@ -397,21 +395,17 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
     if (n && (err = cudaMemsetAsync(f, 0, 4 * (size_t)n, s))) return cuda_status(err);
     return OS2_OK;
   }
-  if (mode == OS2_MODE_FAST) {
-    if ((err = launch_scale_residue(SM_FAST_SCALE, A, lda, m, k, 0, e, nullptr, nullptr, t, status, s)))
-      return cuda_status(err);
-    return cuda_status(
-        launch_scale_residue(SM_FAST_SCALE, B, ldb, n, k, 0, f, nullptr, nullptr, t, status, s));
-  }
+  if (mode == OS2_MODE_FAST)
+    return cuda_status(launch_row_scale(SM_FAST_SCALE, A, lda, m, e, nullptr, nullptr, B, ldb, n,
+                                        f, nullptr, nullptr, k, 0, t, status, s));
   Layout L;
   make_layout(m, n, k, 1, mode, &L);
   if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return OS2_ERR_WORKSPACE;
   int32_t *EA = at<int32_t>(workspace, L.EA), *EB = at<int32_t>(workspace, L.EB);
   int32_t *R = at<int32_t>(workspace, L.R), *K = at<int32_t>(workspace, L.K);
   void *pa = at<void>(workspace, L.planesA), *pb = at<void>(workspace, L.planesB);
-  if ((err = launch_scale_residue(SM_BARS, A, lda, m, k, L.kp, nullptr, EA, pa, t, status, s)))
-    return cuda_status(err);
-  if ((err = launch_scale_residue(SM_BARS, B, ldb, n, k, L.kp, nullptr, EB, pb, t, status, s)))
+  if ((err = launch_row_scale(SM_BARS, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB, pb, k,
+                              L.kp, t, status, s)))
     return cuda_status(err);
   if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)std::max(m, 1), s))) return cuda_status(err);
   if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)std::max(n, 1), s))) return cuda_status(err);
@@ -433,9 +427,8 @@ os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t
   const Os2Tables *t = os2_tables(num_moduli);
   int *status = os2_status_ptr();
   if (!t || !status) return OS2_ERR_CUDA;
-  return cuda_status(launch_scale_residue(SM_RESIDUES, X, ldx, rows, k, ldp,
-                                          const_cast<int32_t *>(exps), nullptr, planes, t, status,
-                                          static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_residues(X, ldx, rows, exps, planes, nullptr, 0, 0, nullptr, nullptr, k,
+                                     ldp, t, static_cast<cudaStream_t>(stream)));
 }
 
 os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB, int ldp,
@@ -568,7 +561,7 @@ int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launch
 int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
   if (m <= 0 || n <= 0 || k < 0 || num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return 0;
   if (k == 0) return 0;
-  return mode == OS2_MODE_ACCURATE ? 9 : 4;
+  return mode == OS2_MODE_ACCURATE ? 7 : 4;
 }
 
 }  // extern "C"

@@ -5,7 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/os2.h"
+#include "os2.h"
 
 #define OS2_MAX_MODULI 20
 #define OS2_KP_ALIGN 64          // residue-plane row pitch granularity (one 128-byte k-block)
@@ -58,18 +58,22 @@ const Os2Tables *os2_tables(int N);
 // Per-device status word (device address), set up on first use.
 int *os2_status_ptr();
 
-// Row-scale / residue kernel modes.
+// Row-scale kernel modes.
 enum ScaleMode {
-  SM_FAST_FUSED = 0,   // e from the revised fast bound, then residue planes
-  SM_RESIDUES = 1,     // residue planes with given exponents
-  SM_FAST_SCALE = 2,   // e only
-  SM_BARS = 3,         // accurate mode: E_i and the 7-bit magnitude plane
+  SM_FAST_SCALE = 0,   // fast mode: e_i from the revised bound
+  SM_BARS = 1,         // accurate mode: E_i and the 7-bit magnitude plane
 };
 
-// Launchers (return cudaError_t of the launch).
-cudaError_t launch_scale_residue(int mode, const double *X, long ldx, int rows, int k, int kp,
-                                 int32_t *e, int32_t *E, void *planes, const Os2Tables *t,
-                                 int *status, cudaStream_t s);
+// Launchers (return cudaError_t of the launch).  Each handles A's rows and
+// B's columns (rows of Bt) in one launch; pass rowsB = 0 for one operand.
+cudaError_t launch_row_scale(int mode, const double *XA, long lda, int rowsA, int32_t *eA,
+                             int32_t *EA, void *barsA, const double *XB, long ldb, int rowsB,
+                             int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
+                             const Os2Tables *t, int *status, cudaStream_t s);
+cudaError_t launch_residues(const double *XA, long lda, int rowsA, const int32_t *eA,
+                            void *planesA, const double *XB, long ldb, int rowsB,
+                            const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
+                            cudaStream_t s);
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,
                                   const Os2Tables *t, cudaStream_t s);
 cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t *e,

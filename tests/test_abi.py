@@ -57,7 +57,7 @@ def test_workspace_sizes():
     h = os2.host_workspace_size(64, 64, 64, 14)
     assert h >= os2.workspace_size(64, 64, 64, 14) + 3 * 64 * 64 * 8
     assert os2.launch_count(64, 64, 64, 14, "fast") == 4
-    assert os2.launch_count(64, 64, 64, 14, "accurate") == 9
+    assert os2.launch_count(64, 64, 64, 14, "accurate") == 7
 
 
 def test_argument_errors_are_synchronous():
