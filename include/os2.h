@@ -67,8 +67,9 @@ typedef enum {
 } os2_mode;
 
 typedef enum {
-  OS2_GEMM_TC = 0,        /* tcgen05 tensor-core kernel (default) */
-  OS2_GEMM_SIMT = 1       /* plain CUDA-core int32 kernel (exact reference, slow) */
+  OS2_GEMM_TC = 0,        /* tcgen05 2-SM tensor-core kernel, 256x256 tiles (default) */
+  OS2_GEMM_SIMT = 1,      /* plain CUDA-core int32 kernel (exact reference, slow) */
+  OS2_GEMM_TC_1SM = 2     /* tcgen05 single-SM tensor-core kernel, 128x256 tiles */
 } os2_gemm_variant;
 
 typedef enum {
@@ -119,7 +120,7 @@ os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t
 /* Step 3 alone: N residue matrix products from FP16 planes RA (N x m x ldp)
  * and RB (N x n x ldp), ldp % 64 == 0, k <= ldp.  out_kind selects int8
  * c_l = sym(G_l mod p_l) or raw int32 G_l; out is [N][m][ldo] with ldo >= n
- * (ldo % 16 == 0 for int8, % 4 for int32).  variant: OS2_GEMM_TC or SIMT.
+ * (ldo % 16 == 0 for int8, % 4 for int32).  variant: an os2_gemm_variant.
  * Raw int32 output with the TC variant runs the exact-accumulation kernel. */
 os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB, int ldp,
                              int num_moduli, int out_kind, void *out, int ldo, int variant,

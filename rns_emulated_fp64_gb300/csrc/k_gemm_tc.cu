@@ -79,8 +79,7 @@ __device__ __forceinline__ void job_coords(int job, const Sched &sp, int &l, int
 
 // The unit sequence every role walks: (job, chunk, TMEM buffer).
 template <int KIND, typename F>
-__device__ __forceinline__ void for_each_unit(const Sched &sp, F &&f) {
-  const int G = gridDim.x, b = blockIdx.x;
+__device__ __forceinline__ void for_each_unit_of(const Sched &sp, int b, int G, F &&f) {
   const int cj = b < sp.njobs ? (sp.njobs - 1 - b) / G + 1 : 0;
   if (KIND == 0) {
     for (int q = 0; q < cj; q += 2) {
@@ -95,6 +94,10 @@ __device__ __forceinline__ void for_each_unit(const Sched &sp, F &&f) {
       for (int c = 0; c < sp.nchunks; c++, u++)
         if (!f(b + q * G, c, u & 1)) return;
   }
+}
+template <int KIND, typename F>
+__device__ __forceinline__ void for_each_unit(const Sched &sp, F &&f) {
+  for_each_unit_of<KIND>(sp, (int)blockIdx.x, (int)gridDim.x, f);
 }
 
 __device__ __forceinline__ void set_status(int *status, int code) {
@@ -380,6 +383,240 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+
+// -------------------------------------------------------------------------
+// 2-SM variant of KIND 0: a CTA pair (cluster of 2) computes a 256x256 tile
+// with tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA loads 128
+// rows of the A tile and 128 rows of the B tile (its half of N) into a
+// 6-stage ring; both CTAs' copies complete on the even CTA's "full" barrier,
+// the MMA commits are multicast to both CTAs' "empty" and "accumulator full"
+// barriers, and both CTAs' epilogues release an accumulator on the even
+// CTA's "accumulator empty" barrier.  Each CTA's TMEM holds its 128 rows x
+// 256 columns of the two interleaved jobs, reduced mod p exactly as in the
+// single-SM kernel.  Per SM this halves the B-tile traffic and lengthens the
+// operand lookahead from 2048 to 3072 MMA cycles.
+constexpr int kStages2 = 6;
+constexpr int kHalf = 128;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm_tc2(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+               const Sched sp, const GemmConsts gc, int8_t *__restrict__ out, int ldo,
+               int *status) {
+  constexpr int BN = 256, STAGES = kStages2;
+  constexpr uint32_t A_BYTES = kHalf * BK * 2, B_BYTES = kHalf * BK * 2;
+  constexpr uint32_t IDESC = idesc_f16_f32(2 * kHalf, BN);
+  constexpr uint32_t TMEM_COLS = 512;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *sA = smem;
+  uint8_t *sB = smem + STAGES * A_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  uint64_t *full = bars, *empty = bars + STAGES;
+  uint64_t *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 2, *mma_done = acc_empty + 2;
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(mma_done + 1);
+  volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 2 * kEpiThreads);
+    }
+    mbar_init(mma_done, 1);
+    *s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) {
+    tmem_alloc2(s_tmem, TMEM_COLS);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive / copy
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producers
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used = 0, last_par = 0;
+      for_each_unit_of<0>(sp, pair, npairs, [&](int job, int c, int) -> bool {
+        int l, tm, tn;
+        job_coords(job, sp, l, tm, tn);
+        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        for (int kb = kb0; kb < kb1; kb++) {
+          if (!mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, s_abort, kWaitLimit)) {
+            *s_abort = 1;
+            set_status(status, OS2_ERR_TIMEOUT);
+            return false;
+          }
+          const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
+          tma_load_3d_pair(sA + stage * A_BYTES, &mapA, fbar, kb * BK,
+                           tm * 2 * kHalf + (int)rank * kHalf, l);
+          tma_load_3d_pair(sB + stage * B_BYTES, &mapB, fbar, kb * BK,
+                           tn * BN + (int)rank * kHalf, l);
+          used |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        return true;
+      });
+      if (leader)
+        for (int s = 0; s < STAGES; s++)
+          if (used >> s & 1) {
+            volatile int no_abort = 0;
+            mbar_wait_cluster_bounded(&full[s], (last_par >> s) & 1, &no_abort, kWaitLimit);
+          }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t aphase[2] = {0, 0};
+      for_each_unit_of<0>(sp, pair, npairs, [&](int, int c, int buf) -> bool {
+        if (!mbar_wait_cluster_bounded(&acc_empty[buf], aphase[buf] ^ 1, s_abort, kWaitLimit)) {
+          *s_abort = 1;
+          set_status(status, OS2_ERR_TIMEOUT);
+          return false;
+        }
+        aphase[buf] ^= 1;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        for (int kb = kb0; kb < kb1; kb++) {
+          if (!mbar_wait_cluster_bounded(&full[stage], phase, s_abort, kWaitLimit)) {
+            *s_abort = 1;
+            set_status(status, OS2_ERR_TIMEOUT);
+            return false;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_k128(smem_u32(sA + stage * A_BYTES));
+          const uint64_t bd = sdesc_k128(smem_u32(sB + stage * B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; kk++) {
+            const uint32_t acc = (kb > kb0 || kk > 0 || c > 0) ? 1u : 0u;
+            umma2_f16(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
+          }
+          umma2_commit_mc(&empty[stage], 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        umma2_commit_mc(&acc_full[buf], 0x3);
+        return true;
+      });
+      umma2_commit_mc(mma_done, 0x1);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(mma_done, 0, &no_abort, kWaitLimit);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int r_in_tile = quarter * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t empty_leader[2] = {mapa_shared(smem_u32(&acc_empty[0]), 0),
+                                      mapa_shared(smem_u32(&acc_empty[1]), 0)};
+    uint32_t aphase[2] = {0, 0};
+    for_each_unit_of<0>(sp, pair, npairs, [&](int job, int c, int buf) -> bool {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(&acc_full[buf], aphase[buf],
+                                                                         s_abort, kWaitLimit));
+      if (!ok) {
+        *s_abort = 1;
+        set_status(status, OS2_ERR_TIMEOUT);
+        return false;
+      }
+      aphase[buf] ^= 1;
+      tc_fence_after();
+      int l, tm, tn;
+      job_coords(job, sp, l, tm, tn);
+      const float p = gc.p[l], invp = gc.invp[l];
+      const uint32_t taddr = lane_base + (uint32_t)(buf * BN);
+      if (c != sp.nchunks - 1) {
+#pragma unroll 1
+        for (int g = 0; g < BN / 32; g++) {
+          uint32_t v[32];
+          tmem_ld32(taddr + g * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            const float x = __uint_as_float(v[i]);
+            v[i] = __float_as_uint(fmaf(-p, rintf(x * invp), x));
+          }
+          tmem_st32(taddr + g * 32, v);
+        }
+        tmem_wait_st();
+      } else {
+        const float hi = gc.hi[l], lo = gc.lo[l];
+        const int grow = tm * 2 * kHalf + (int)rank * kHalf + r_in_tile;
+        const int col0 = tn * BN;
+        int8_t *dst = out + ((size_t)l * sp.m + grow) * (size_t)ldo + col0;
+#pragma unroll 1
+        for (int g = 0; g < BN / 32; g++) {
+          uint32_t v[32];
+          tmem_ld32(taddr + g * 32, v);
+          tmem_wait_ld();
+          uint32_t packed[8];
+#pragma unroll
+          for (int i = 0; i < 8; i++) packed[i] = 0;
+#pragma unroll
+          for (int i = 0; i < 32; i++) {
+            const float x = __uint_as_float(v[i]);
+            float r = fmaf(-p, rintf(x * invp), x);
+            r = r > hi ? r - p : r;
+            r = r < lo ? r + p : r;
+            packed[i >> 2] |= ((uint32_t)(int)r & 0xFFu) << (8 * (i & 3));
+          }
+          if (grow < sp.m) {
+            const int cb = col0 + g * 32;
+            if (cb + 32 <= sp.n) {
+              uint4 *d4 = reinterpret_cast<uint4 *>(dst + g * 32);
+              d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            } else {
+              for (int i = 0; i < 32 && cb + i < sp.n; i++)
+                dst[g * 32 + i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(empty_leader[buf]);
+      return true;
+    });
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still touch its shared memory or TMEM
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, TMEM_COLS);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -453,12 +690,44 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
   return cudaGetLastError();
 }
 
+cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
+                    int ldo, const Os2Tables *t, int *status, cudaStream_t s) {
+  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, RA, kp, m, nplanes, kHalf) || !make_map(&mb, RB, kp, n, nplanes, kHalf))
+    return cudaErrorInvalidValue;
+  Sched sp;
+  sp.m = m;
+  sp.n = n;
+  sp.kb_total = kp / BK;
+  sp.tiles_m = (m + 2 * kHalf - 1) / (2 * kHalf);
+  sp.tiles_n = (n + 255) / 256;
+  sp.tiles = sp.tiles_m * sp.tiles_n;
+  sp.njobs = sp.tiles * nplanes;
+  sp.chunk = (int)(((1LL << 24) - 135) / ((long long)BK << 14));
+  sp.nchunks = (sp.kb_total + sp.chunk - 1) / sp.chunk;
+  if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
+  const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
+  GemmConsts gc = t ? t->gemm : GemmConsts{};
+  k_gemm_tc2<<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, gc, reinterpret_cast<int8_t *>(out), ldo,
+                                               status);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
                            int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,
                            int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s) {
   if (m <= 0 || n <= 0 || kp <= 0) return cudaSuccess;
+  if (kind == 2) return launch2(m, n, kp, RA, RB, nplanes, out, ldo, t, status, s);
   if (kind == 0)
     return launch<0>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
                      status, s);

@@ -299,11 +299,12 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
   // step 3
   {
     ProfScope ps("gemm_modp", s);
-    if (g_variant.load() == OS2_GEMM_SIMT)
+    const int variant = g_variant.load();
+    if (variant == OS2_GEMM_SIMT)
       err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
     else
-      err = launch_gemm_tc(0, m, n, L.kp, pa, pb, N, cres, L.ldcres, nullptr, nullptr, 14, t,
-                           status, s);
+      err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : 2, m, n, L.kp, pa, pb, N, cres,
+                           L.ldcres, nullptr, nullptr, 14, t, status, s);
     if (err) return cuda_status(err);
   }
   // steps 4 + 5
@@ -437,7 +438,8 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
   if (m < 0 || n < 0 || k < 0 || k > ldp || ldp % OS2_KP_ALIGN) return OS2_ERR_INVALID_ARG;
   if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
   if (out_kind != OS2_OUT_MODP_INT8 && out_kind != OS2_OUT_RAW_INT32) return OS2_ERR_INVALID_ARG;
-  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT) return OS2_ERR_INVALID_ARG;
+  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM)
+    return OS2_ERR_INVALID_ARG;
   if (ldo < std::max(n, 1)) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_MODP_INT8 && ldo % OS2_CRES_ALIGN) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_RAW_INT32 && ldo % 4) return OS2_ERR_INVALID_ARG;
@@ -456,8 +458,9 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
   if (!t || !status) return OS2_ERR_CUDA;
   if (variant == OS2_GEMM_SIMT)
     return cuda_status(launch_gemm_simt(m, n, ldp, RA, RB, num_moduli, out_kind, out, ldo, t, s));
-  return cuda_status(launch_gemm_tc(out_kind == OS2_OUT_MODP_INT8 ? 0 : 1, m, n, ldp, RA, RB,
-                                    num_moduli, out, ldo, nullptr, nullptr, 14, t, status, s));
+  const int kind = out_kind == OS2_OUT_RAW_INT32 ? 1 : (variant == OS2_GEMM_TC_1SM ? 0 : 2);
+  return cuda_status(launch_gemm_tc(kind, m, n, ldp, RA, RB, num_moduli, out, ldo, nullptr, nullptr,
+                                    14, t, status, s));
 }
 
 os2_status os2_crt(int m, int n, const int8_t *c, int ldcres, int num_moduli, const int32_t *e,
@@ -491,7 +494,8 @@ os2_status os2_get_status(void *stream) {
 }
 
 os2_status os2_set_gemm_variant(int variant) {
-  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT) return OS2_ERR_INVALID_ARG;
+  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM)
+    return OS2_ERR_INVALID_ARG;
   g_variant.store(variant);
   return OS2_OK;
 }

@@ -82,8 +82,8 @@ cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t 
 cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *RB, int N,
                              int out_kind, void *out, int ldo, const Os2Tables *t, cudaStream_t s);
 
-// tcgen05 GEMM.  kind: 0 = mod-p int8 output, 1 = exact int32 (raw output and/or
-// row/col maxima).  prod_bound_log2: log2 of the largest |a*b| of one term
+// tcgen05 GEMM.  kind: 0 = mod-p int8 output (single SM), 1 = exact int32 (raw
+// output and/or row/col maxima), 2 = mod-p int8 output on SM pairs (2-SM MMA).  prod_bound_log2: log2 of the largest |a*b| of one term
 // (14 for residues, 12 for the accurate-mode magnitude planes).
 cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
                            int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,

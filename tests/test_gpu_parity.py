@@ -124,8 +124,8 @@ def test_raw_int32_products_bit_exact(variant, m, n, k):
     assert np.array_equal(G.cpu().numpy()[:, :, :n].astype(np.int64), want)
 
 
-@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_SIMT])
-@pytest.mark.parametrize("m,n,k,N", [(128, 256, 64, 2), (129, 257, 65, 14), (300, 520, 1000, 16),
+@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_TC_1SM, os2.GEMM_SIMT])
+@pytest.mark.parametrize("m,n,k,N", [(128, 256, 64, 2), (513, 700, 3000, 16), (256, 256, 961, 5), (129, 257, 65, 14), (300, 520, 1000, 16),
                                      (256, 512, 2000, 20), (70, 33, 3000, 9)])
 def test_modp_products_bit_exact(variant, m, n, k, N):
     A, Bt, e, f, RA, RB = _planes_pair(m, n, k, N, seed=m)
@@ -147,9 +147,10 @@ def test_int32_accumulation_worst_case():
     G = os2.gemm_residues(RA, RB, k, os2.OUT_RAW_INT32, os2.GEMM_TC)
     status_ok()
     assert torch.all(G[:, :, :128] == 16384 * k)
-    c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC)
-    status_ok()
-    assert torch.all(c[:, :, :128] == 0)       # 2^14 k is a multiple of 256
+    for variant in (os2.GEMM_TC, os2.GEMM_TC_1SM):
+        c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, variant)
+        status_ok()
+        assert torch.all(c[:, :, :128] == 0)   # 2^14 k is a multiple of 256
 
 
 def test_modp_alternating_extremes():
@@ -166,7 +167,9 @@ def test_modp_alternating_extremes():
         rb[l] = rng.choice([lo, hi], size=(n, k))
     RA, RB = dev(ra), dev(rb)
     c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC).cpu().numpy()[:, :, :n]
+    c1 = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC_1SM).cpu().numpy()[:, :, :n]
     status_ok()
+    assert np.array_equal(c, c1)
     G = np.einsum("lik,ljk->lij", ra.astype(np.int64), rb.astype(np.int64))
     for l, p in enumerate(mods):
         r = np.mod(G[l], p)
@@ -243,16 +246,17 @@ def test_gemm_64cube_normal_config():
     assert_bits_equal(C, ref.C, "64^3")
 
 
-def test_simt_variant_end_to_end():
+@pytest.mark.parametrize("variant", [os2.GEMM_SIMT, os2.GEMM_TC_1SM])
+def test_gemm_variants_end_to_end(variant):
     A, Bt = workloads.make_pair("spread", 150, 170, 400, seed=1, phi=2.0)
     try:
-        os2.set_gemm_variant(os2.GEMM_SIMT)
+        os2.set_gemm_variant(variant)
         Cs = os2.gemm(dev(A), dev(Bt), 16).cpu().numpy()
     finally:
         os2.set_gemm_variant(os2.GEMM_TC)
     Ct = os2.gemm(dev(A), dev(Bt), 16).cpu().numpy()
     status_ok()
-    assert_bits_equal(Cs, Ct, "simt vs tc")
+    assert_bits_equal(Cs, Ct, "variant vs default tc")
     ref = orc.gemm_entries(A, Bt, 16, want_X=False, want_c=False, want_G=False)
     assert_bits_equal(Ct, ref.C, "tc vs oracle")
 
