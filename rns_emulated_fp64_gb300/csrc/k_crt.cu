@@ -5,46 +5,76 @@
 // inv_l = M_l^-1 mod p_l.  [Q] "高い精度での復元(手順4)": P reaches 2^125 at 16
 // moduli, beyond double and int64, so this step needs more precision.  GB300's
 // FP64 rate is low, so instead of the double-double arithmetic the article
-// describes, X is computed exactly in integer limbs:
-//   S_u = sum_l c_l W_l,u  (16-bit limbs of W_l; |S_u| < 2^31, no carries yet)
-//   q   = rint(sum_l c_l fl(inv_l / p_l))   (FP32; the exact S/P = sum c_l inv_l/p_l)
-//   X   = S - q P, carries propagated once; a one-step correction if the FP32
-//         estimate was within 0.01 of a half-integer.
+// describes, X is computed exactly in 32-bit integer limbs:
+//   Y_u = sum_l (c_l + 128) W_l,u      unsigned 64-bit sums, no carries yet
+//   Y   = sum_u Y_u 2^(32u) = S + K,   S = sum_l c_l W_l, K = 128 sum_l W_l
+//   q   = nearest integer to (Y - K) / P, estimated in FP32 from the two
+//         highest limb sums (error below 0.003)
+//   X   = Y - K - q P, carries propagated once; if the estimate was within
+//         0.01 of a half-integer, one exact comparison with P/2 fixes q.
 // X lies in [-P/2, P/2).  [Q] "2の累乗による整数化(手順1と5)": C_ij = X_ij 2^-(e_i+f_j),
 // rounded once to nearest-even from the exact integer (subnormals, overflow).
 //
 // One thread per 4 consecutive entries of a row: each residue plane is read
-// with one 4-byte load per thread (coalesced), C with 8-byte stores.
+// with one 4-byte load per thread (coalesced).
 #include "os2_internal.cuh"
 
 namespace {
 
 constexpr int kThreads = 128;
 
-// RN-even of (w2:w1:w0) * 2^-s, sign `neg`; mirrors IEEE-754 binary64.
-__device__ __forceinline__ double round_scaled(uint64_t w0, uint64_t w1, uint64_t w2, bool neg,
-                                               int s) {
-  if ((w0 | w1 | w2) == 0) return 0.0;
-  const uint64_t w[4] = {w0, w1, w2, 0};
-  int b = w2 ? 128 + 64 - __clzll((long long)w2)
-             : (w1 ? 64 + 64 - __clzll((long long)w1) : 64 - __clzll((long long)w0));
+// 32-bit limbs of P (and of every W_l < P): each group of four moduli of the
+// table adds just under 32 bits (bit lengths 32, 64, 95, 126, 156 at N = 4,
+// 8, 12, 16, 20), so (N + 3) / 4 limbs hold P; one more holds Y < 256 N P.
+template <int N>
+struct Limbs {
+  static constexpr int LW = (N + 3) / 4;
+  static constexpr int LX = LW + 1;
+};
+
+// RN-even of |X| * 2^-s with |X| in 32-bit limbs m[0..L), sign `neg`.
+template <int L>
+__device__ __forceinline__ double round_scaled(const uint32_t (&m)[L], bool neg, int s) {
+  int top = -1;
+#pragma unroll
+  for (int u = 0; u < L; u++)
+    if (m[u]) top = u;
+  if (top < 0) return 0.0;
+  uint32_t mt = 0;
+#pragma unroll
+  for (int u = 0; u < L; u++)
+    if (u == top) mt = m[u];
+  const int b = 32 * top + 32 - __clz(mt);  // bit length of |X|
   int cut = max(b - 53, s - 1074);
   uint64_t kept;
   if (cut <= 0) {
-    kept = w0;
+    kept = (uint64_t)m[0] | (L > 1 ? (uint64_t)m[L > 1 ? 1 : 0] << 32 : 0ull);
     cut = 0;
   } else if (cut > b) {
     kept = 0;
   } else {
-    const int idx = cut >> 6, off = cut & 63;
-    kept = w[idx] >> off;
-    if (off && idx + 1 < 4) kept |= w[idx + 1] << (64 - off);
-    const int rb = cut - 1;  // round bit position
-    const uint64_t round = (w[rb >> 6] >> (rb & 63)) & 1;
+    // bits [cut, cut + 54) of |X|, round bit cut - 1, sticky below
+    const int w = cut >> 5, o = cut & 31;
+    uint32_t a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+    for (int u = 0; u < L; u++) {
+      if (u == w) a0 = m[u];
+      if (u == w + 1) a1 = m[u];
+      if (u == w + 2) a2 = m[u];
+    }
+    const uint64_t lo64 = (uint64_t)a0 | ((uint64_t)a1 << 32);
+    kept = (lo64 >> o) | (o ? ((uint64_t)a2 << (64 - o)) : 0ull);
+    const int rb = cut - 1;
+    const int rw = rb >> 5, ro = rb & 31;
+    uint32_t rwv = 0;
     bool sticky = false;
-    const int sw = rb >> 6, sb = rb & 63;  // bits [0, rb)
-    for (int i = 0; i < sw; i++) sticky |= w[i] != 0;
-    if (sb) sticky |= (w[sw] & ((1ull << sb) - 1)) != 0;
+#pragma unroll
+    for (int u = 0; u < L; u++) {
+      if (u == rw) rwv = m[u];
+      if (u < rw) sticky |= m[u] != 0;
+    }
+    const uint32_t round = (rwv >> ro) & 1u;
+    sticky |= (rwv & ((1u << ro) - 1u)) != 0;
     if (round && (sticky || (kept & 1))) kept++;
   }
   if (kept == 0) return neg ? -0.0 : 0.0;
@@ -71,23 +101,26 @@ __global__ void __launch_bounds__(kThreads)
     k_crt(int m, int n, int groups, const int8_t *__restrict__ c, int ldcres,
           const int32_t *__restrict__ e, const int32_t *__restrict__ f, double *__restrict__ C,
           int ldc, uint32_t *__restrict__ Xout, const CrtConsts cc) {
+  constexpr int LW = Limbs<N>::LW, LX = Limbs<N>::LX;
   const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
   if (gid >= (long long)m * groups) return;
   const int i = (int)(gid / groups);
   const int j0 = (int)(gid - (long long)i * groups) * 4;
 
-  int32_t r4[N];
+  // residues + 128 of 4 entries per modulus, one byte each
+  uint32_t r4[N];
   const size_t plane = (size_t)m * ldcres;
   const int8_t *src = c + (size_t)i * ldcres + j0;
   if (j0 + 4 <= n) {
 #pragma unroll
-    for (int l = 0; l < N; l++) r4[l] = __ldg(reinterpret_cast<const int32_t *>(src + l * plane));
+    for (int l = 0; l < N; l++)
+      r4[l] = __ldg(reinterpret_cast<const uint32_t *>(src + l * plane)) ^ 0x80808080u;
   } else {
 #pragma unroll
     for (int l = 0; l < N; l++) {
       uint32_t v = 0;
       for (int u = 0; u < 4 && j0 + u < n; u++) v |= (uint32_t)(uint8_t)src[l * plane + u] << (8 * u);
-      r4[l] = (int32_t)v;
+      r4[l] = v ^ 0x80808080u;
     }
   }
   const int ei = e[i];
@@ -96,80 +129,78 @@ __global__ void __launch_bounds__(kThreads)
   for (int u = 0; u < 4; u++) {
     const int j = j0 + u;
     if (j >= n) break;
-    float t = 0.f;
-    int acc[OS2_CRT_LIMBS];
+    // Y_v = sum_l (c_l + 128) W_l,v
+    uint64_t Y[LW];
 #pragma unroll
-    for (int v = 0; v < OS2_CRT_LIMBS; v++) acc[v] = 0;
+    for (int v = 0; v < LW; v++) Y[v] = 0;
 #pragma unroll
     for (int l = 0; l < N; l++) {
-      const int cl = (int)(int8_t)((uint32_t)r4[l] >> (8 * u));
-      t = fmaf((float)cl, cc.phi[l], t);
+      const uint32_t cl = (r4[l] >> (8 * u)) & 0xFFu;
 #pragma unroll
-      for (int v = 0; v < OS2_CRT_LIMBS; v++) acc[v] += cl * cc.W16[l][v];
+      for (int v = 0; v < LW; v++) Y[v] += (uint64_t)cl * cc.W32[l][v];
     }
+    // q = round((Y - K) / P) from the two top limb sums
+    float t = (float)Y[LW - 1] * cc.s_top - cc.KoverP;
+    if (LW > 1) t = fmaf((float)Y[LW > 1 ? LW - 2 : 0], cc.s_next, t);
     const float qf = rintf(t);
     const int q = (int)qf;
+    // X = Y - K - q P in signed 64-bit limb sums, then one carry pass
+    uint32_t x[LX];
+    long long carry = 0;
 #pragma unroll
-    for (int v = 0; v < OS2_CRT_LIMBS; v++) acc[v] -= q * cc.P16[v];
-    uint32_t x16[OS2_CRT_LIMBS];
-    int carry = 0;
-#pragma unroll
-    for (int v = 0; v < OS2_CRT_LIMBS; v++) {
-      const int sv = acc[v] + carry;
-      x16[v] = (uint32_t)sv & 0xFFFFu;
-      carry = sv >> 16;
+    for (int v = 0; v < LX; v++) {
+      const long long yv = v < LW ? (long long)Y[v < LW ? v : 0] : 0ll;
+      const long long sv = yv - (long long)cc.K32[v] - (long long)q * (long long)cc.P32[v] + carry;
+      x[v] = (uint32_t)sv;
+      carry = sv >> 32;
     }
-    // |t - S/P| < 0.003, so X is already in [-P/2, P/2) unless the estimate
-    // was near a half-integer; then compare with P/2 exactly.
+    // X is far inside the 32*LX-bit window, so its sign is the top bit of
+    // x[LX-1].  The quotient can be off by one only when the estimate sat
+    // within 0.01 of a half-integer; then compare X with +-P/2 exactly.
     const float fr = t - qf;
-    if (fr > 0.49f) {
-      int cr = 0;
-      for (int v = 0; v < OS2_CRT_LIMBS; v++) cr = ((int)x16[v] - cc.half16[v] + cr) >> 16;
-      if (carry + cr >= 0) {  // X >= P/2: X -= P
-        cr = 0;
-        for (int v = 0; v < OS2_CRT_LIMBS; v++) {
-          const int sv = (int)x16[v] - cc.P16[v] + cr;
-          x16[v] = (uint32_t)sv & 0xFFFFu;
-          cr = sv >> 16;
-        }
-        carry += cr;
+    if (fr > 0.49f || fr < -0.49f) {
+      const bool up = fr > 0.49f;  // X may be >= P/2 (then X -= P); else X may be < -P/2
+      long long cr = 0;
+      uint32_t last = 0;
+#pragma unroll
+      for (int v = 0; v < LX; v++) {
+        const long long dv =
+            (long long)x[v] + (up ? -(long long)cc.H32[v] : (long long)cc.H32[v]) + cr;
+        last = (uint32_t)dv;
+        cr = dv >> 32;
       }
-    } else if (fr < -0.49f) {
-      int cr = 0;
-      for (int v = 0; v < OS2_CRT_LIMBS; v++) cr = ((int)x16[v] + cc.half16[v] + cr) >> 16;
-      if (carry + cr < 0) {  // X < -P/2: X += P
-        cr = 0;
-        for (int v = 0; v < OS2_CRT_LIMBS; v++) {
-          const int sv = (int)x16[v] + cc.P16[v] + cr;
-          x16[v] = (uint32_t)sv & 0xFFFFu;
-          cr = sv >> 16;
+      const bool dneg = (int32_t)last < 0;  // sign of X -+ P/2
+      if (up ? !dneg : dneg) {
+        long long cr2 = 0;
+#pragma unroll
+        for (int v = 0; v < LX; v++) {
+          const long long sv =
+              (long long)x[v] + (up ? -(long long)cc.P32[v] : (long long)cc.P32[v]) + cr2;
+          x[v] = (uint32_t)sv;
+          cr2 = sv >> 32;
         }
-        carry += cr;
       }
     }
-    const bool neg = carry < 0;
-    uint64_t w0 = (uint64_t)x16[0] | ((uint64_t)x16[1] << 16) | ((uint64_t)x16[2] << 32) |
-                  ((uint64_t)x16[3] << 48);
-    uint64_t w1 = (uint64_t)x16[4] | ((uint64_t)x16[5] << 16) | ((uint64_t)x16[6] << 32) |
-                  ((uint64_t)x16[7] << 48);
-    uint64_t w2 = (uint64_t)x16[8] | ((uint64_t)x16[9] << 16);
-    if (neg) w2 |= 0xFFFFFFFF00000000ull;  // sign-extend the 160-bit value to 192 bits
+    const bool neg = (int32_t)x[LX - 1] < 0;
     if (Xout) {
       uint32_t *xo = Xout + ((size_t)i * n + j) * 8;
-      xo[0] = (uint32_t)w0; xo[1] = (uint32_t)(w0 >> 32);
-      xo[2] = (uint32_t)w1; xo[3] = (uint32_t)(w1 >> 32);
-      xo[4] = (uint32_t)w2; xo[5] = (uint32_t)(w2 >> 32);
-      xo[6] = neg ? 0xFFFFFFFFu : 0u; xo[7] = neg ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+      for (int v = 0; v < 8; v++) xo[v] = v < LX ? x[v < LX ? v : 0] : (neg ? 0xFFFFFFFFu : 0u);
     }
-    if (neg) {  // magnitude = two's complement
-      w0 = ~w0; w1 = ~w1; w2 = ~w2;
-      w0 += 1;
-      const uint64_t c0 = w0 == 0;
-      w1 += c0;
-      const uint64_t c1 = c0 & (w1 == 0);
-      w2 += c1;
+    uint32_t mag[LX];
+    if (neg) {
+      uint64_t cy = 1;
+#pragma unroll
+      for (int v = 0; v < LX; v++) {
+        cy += (uint64_t)(~x[v]);
+        mag[v] = (uint32_t)cy;
+        cy >>= 32;
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < LX; v++) mag[v] = x[v];
     }
-    C[(size_t)i * ldc + j] = round_scaled(w0, w1, w2, neg, ei + f[j]);
+    C[(size_t)i * ldc + j] = round_scaled<LX>(mag, neg, ei + f[j]);
   }
 }
 

@@ -1,6 +1,7 @@
 // libos2 host side: the C ABI declared in include/os2.h, argument checking,
 // workspace layout, constant tables and the launch sequence of the five steps.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <string.h>
 
 #include <algorithm>
@@ -86,7 +87,21 @@ int u_bitlen(const U256 &a) {
     if (a.w[i]) return 32 * i + 32 - __builtin_clz(a.w[i]);
   return 0;
 }
-uint32_t limb16(const U256 &a, int v) { return (a.w[v / 2] >> (16 * (v % 2))) & 0xFFFFu; }
+U256 u_add(const U256 &a, const U256 &b) {
+  U256 r;
+  uint64_t c = 0;
+  for (int i = 0; i < 8; i++) {
+    c += (uint64_t)a.w[i] + b.w[i];
+    r.w[i] = (uint32_t)c;
+    c >>= 32;
+  }
+  return r;
+}
+double u_to_double(const U256 &a) {
+  double r = 0;
+  for (int i = 7; i >= 0; i--) r = r * 4294967296.0 + (double)a.w[i];
+  return r;
+}
 
 // a^-1 mod p by the extended Euclidean algorithm (a, p coprime)
 int inv_mod(int a, int p) {
@@ -115,6 +130,7 @@ void build_tables(int N, Os2Tables *t) {
   const U256 H = u_shr1(u_sub1(P));  // floor((P-1)/2)
   const U256 half = u_shr1(P);       // P/2 (P is even: 256 is a modulus)
   t->res.N = t->crt.N = t->gemm.N = N;
+  U256 Ksum = u_from(0);
   for (int l = 0; l < N; l++) {
     const int p = kModuli[l];
     t->p[l] = p;
@@ -133,13 +149,22 @@ void build_tables(int N, Os2Tables *t) {
       t->res.w12[l][u] = (float)sym(pw, p);
       pw = (int)(((long long)pw * 4096) % p);
     }
-    t->crt.phi[l] = (float)((double)t->inv[l] / (double)p);
-    for (int v = 0; v < OS2_CRT_LIMBS; v++) t->crt.W16[l][v] = (int32_t)limb16(W, v);
+    for (int v = 0; v < 5; v++) t->crt.W32[l][v] = W.w[v];
+    Ksum = u_add(Ksum, W);
   }
-  for (int v = 0; v < OS2_CRT_LIMBS; v++) {
-    t->crt.P16[v] = (int32_t)limb16(P, v);
-    t->crt.half16[v] = (int32_t)limb16(half, v);
+  const U256 K = u_mul(Ksum, 128);
+  for (int v = 0; v < 6; v++) {
+    t->crt.P32[v] = P.w[v];
+    t->crt.K32[v] = K.w[v];
+    t->crt.H32[v] = half.w[v];
   }
+  const int LW = (N + 3) / 4;
+  const double Pd = u_to_double(P);
+  t->crt.s_top = (float)(ldexp(1.0, 32 * (LW - 1)) / Pd);
+  t->crt.s_next = (float)(LW > 1 ? ldexp(1.0, 32 * (LW - 2)) / Pd : 0.0);
+  double kop = 0;
+  for (int l = 0; l < N; l++) kop += 128.0 * t->inv[l] / (double)kModuli[l];
+  t->crt.KoverP = (float)kop;
   for (int i = 0; i < OS2_H_LIMBS; i++) t->res.H[i] = H.w[i];
   t->res.bitlenH = u_bitlen(H);
 }

@@ -11,7 +11,6 @@
 #define OS2_KP_ALIGN 64          // residue-plane row pitch granularity (one 128-byte k-block)
 #define OS2_CRES_ALIGN 16        // int8 product-residue row pitch granularity
 #define OS2_H_LIMBS 7            // 32-bit limbs for H (P < 2^156 for N <= 20)
-#define OS2_CRT_LIMBS 10         // 16-bit limbs for the CRT sums (160 bits)
 
 // Step-2 constants (kernel parameter, lives in the constant bank).
 struct ResConsts {
@@ -25,13 +24,15 @@ struct ResConsts {
   int bitlenH;
 };
 
-// Steps 4-5 constants.
+// Steps 4-5 constants (32-bit little-endian limbs).
 struct CrtConsts {
   int N;
-  float phi[OS2_MAX_MODULI];                      // fl(inv_l / p_l) = fl(W_l / P)
-  int32_t W16[OS2_MAX_MODULI][OS2_CRT_LIMBS];     // W_l = M_l inv_l in 16-bit limbs
-  int32_t P16[OS2_CRT_LIMBS];                     // P in 16-bit limbs
-  int32_t half16[OS2_CRT_LIMBS];                  // P/2 in 16-bit limbs
+  uint32_t W32[OS2_MAX_MODULI][5];   // W_l = M_l inv_l
+  uint32_t P32[6];                   // P
+  uint32_t K32[6];                   // K = 128 sum_l W_l (offset of the unsigned residues)
+  uint32_t H32[6];                   // P / 2
+  float s_top, s_next;               // fl(2^(32(LW-1)) / P), fl(2^(32(LW-2)) / P), LW = (N+3)/4
+  float KoverP;                      // fl(K / P)
 };
 
 // Step-3 constants.

@@ -178,7 +178,7 @@ def test_modp_alternating_extremes():
 
 
 # --------------------------------------------------------------- steps 4-5 --
-@pytest.mark.parametrize("N", [2, 12, 14, 16, 20])
+@pytest.mark.parametrize("N", [1, 2, 4, 5, 8, 9, 12, 13, 14, 16, 17, 20])
 def test_crt_parity_from_oracle_residues(N):
     A, Bt = workloads.make_pair("spread", 37, 45, 90, seed=N, phi=2.0)
     ref = orc.gemm_entries(A, Bt, N)
@@ -194,7 +194,7 @@ def test_crt_random_residues_and_rounding():
     """Arbitrary residue vectors (X anywhere in [-P/2, P/2)) and exponents that
     push the result into the subnormal and overflow ranges."""
     rng = np.random.default_rng(2)
-    for N in (1, 3, 16, 20):
+    for N in (1, 3, 4, 5, 8, 9, 12, 13, 16, 17, 20):
         mods = os2.moduli(N)
         m, n = 33, 65
         cres = np.zeros((N, m, 80), np.int8)
