@@ -32,9 +32,10 @@ struct Limbs {
   static constexpr int LX = LW + 1;
 };
 
-// RN-even of |X| * 2^-s with |X| in 32-bit limbs m[0..L), sign `neg`.
+// RN-even of |X| * 2^-s with |X| in 32-bit limbs m[0..L), sign `neg`
+// (general routine: zero, subnormal and overflowing results; kept out of line).
 template <int L>
-__device__ __forceinline__ double round_scaled(const uint32_t (&m)[L], bool neg, int s) {
+__device__ __noinline__ double round_scaled(const uint32_t (&m)[L], bool neg, int s) {
   int top = -1;
 #pragma unroll
   for (int u = 0; u < L; u++)
@@ -96,16 +97,60 @@ __device__ __forceinline__ double round_scaled(const uint32_t (&m)[L], bool neg,
   return __longlong_as_double((long long)bits);
 }
 
+
+// Normal-range fast path of round_scaled: the top three nonzero-anchored limbs
+// hold at least 65 significant bits, enough for 53 bits, the round bit and a
+// sticky bit (OR-ed with everything below).  Falls back to the general routine
+// for zero, subnormal or overflowing results.
+template <int L>
+__device__ __forceinline__ double round_scaled_fast(const uint32_t (&m)[L], bool neg, int s) {
+  int t = -1;
+#pragma unroll
+  for (int u = 0; u < L; u++)
+    if (m[u]) t = u;
+  uint32_t hi = 0, mid = 0, lo = 0;
+  bool rest = false;
+#pragma unroll
+  for (int u = 0; u < L; u++) {
+    if (u == t) hi = m[u];
+    if (u == t - 1) mid = m[u];
+    if (u == t - 2) lo = m[u];
+    if (u < t - 2) rest |= m[u] != 0;
+  }
+  const int lz = __clz(hi);
+  const int etop = 32 * t + 31 - lz - s;  // exponent of the leading bit of |X| 2^-s
+  if (t < 0 || etop < -1022 || etop > 1023) return round_scaled<L>(m, neg, s);
+  const uint32_t t1 = __funnelshift_l(mid, hi, lz);
+  const uint32_t t0 = __funnelshift_l(lo, mid, lz);
+  const uint32_t tail = lo << lz;  // bits below the 64-bit window (lz < 32)
+  const uint64_t T = ((uint64_t)t1 << 32) | t0;
+  uint64_t kept = T >> 11;  // 53 bits, leading bit set
+  const bool round = (T >> 10) & 1;
+  const bool sticky = (T & 0x3FFull) != 0 || tail != 0 || rest;
+  int ex = etop;
+  if (round && (sticky || (kept & 1))) {
+    kept++;
+    if (kept >> 53) {
+      kept >>= 1;
+      ex++;
+    }
+  }
+  uint64_t bits = ex > 1023 ? 0x7FF0000000000000ull
+                            : (((uint64_t)(ex + 1023) << 52) | (kept & ((1ull << 52) - 1)));
+  if (neg) bits |= 1ull << 63;
+  return __longlong_as_double((long long)bits);
+}
+
 template <int N>
 __global__ void __launch_bounds__(kThreads)
     k_crt(int m, int n, int groups, const int8_t *__restrict__ c, int ldcres,
           const int32_t *__restrict__ e, const int32_t *__restrict__ f, double *__restrict__ C,
           int ldc, uint32_t *__restrict__ Xout, const CrtConsts cc) {
   constexpr int LW = Limbs<N>::LW, LX = Limbs<N>::LX;
-  const long long gid = (long long)blockIdx.x * kThreads + threadIdx.x;
-  if (gid >= (long long)m * groups) return;
-  const int i = (int)(gid / groups);
-  const int j0 = (int)(gid - (long long)i * groups) * 4;
+  const int g = blockIdx.x * kThreads + threadIdx.x;
+  if (g >= groups) return;
+  const int j0 = g * 4;
+  for (int i = blockIdx.y; i < m; i += gridDim.y) {
 
   // residues + 128 of 4 entries per modulus, one byte each
   uint32_t r4[N];
@@ -129,13 +174,14 @@ __global__ void __launch_bounds__(kThreads)
   for (int u = 0; u < 4; u++) {
     const int j = j0 + u;
     if (j >= n) break;
+    const uint32_t sel = 0x4440u | (uint32_t)u;  // byte u, zero-extended
     // Y_v = sum_l (c_l + 128) W_l,v
     uint64_t Y[LW];
 #pragma unroll
     for (int v = 0; v < LW; v++) Y[v] = 0;
 #pragma unroll
     for (int l = 0; l < N; l++) {
-      const uint32_t cl = (r4[l] >> (8 * u)) & 0xFFu;
+      const uint32_t cl = __byte_perm(r4[l], 0u, sel);
 #pragma unroll
       for (int v = 0; v < LW; v++) Y[v] += (uint64_t)cl * cc.W32[l][v];
     }
@@ -200,7 +246,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int v = 0; v < LX; v++) mag[v] = x[v];
     }
-    C[(size_t)i * ldc + j] = round_scaled<LX>(mag, neg, ei + f[j]);
+    C[(size_t)i * ldc + j] = round_scaled_fast<LX>(mag, neg, ei + f[j]);
+  }
   }
 }
 
@@ -211,11 +258,10 @@ cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t 
                        cudaStream_t s) {
   if (m <= 0 || n <= 0) return cudaSuccess;
   const int groups = (n + 3) / 4;
-  const long long total = (long long)m * groups;
-  const unsigned blocks = (unsigned)((total + kThreads - 1) / kThreads);
-#define OS2_CASE(NN)                                                                         \
-  case NN:                                                                                   \
-    k_crt<NN><<<blocks, kThreads, 0, s>>>(m, n, groups, c, ldcres, e, f, C, ldc, X_out, t->crt); \
+  const dim3 grid((groups + kThreads - 1) / kThreads, m < 65535 ? m : 65535);
+#define OS2_CASE(NN)                                                                       \
+  case NN:                                                                                 \
+    k_crt<NN><<<grid, kThreads, 0, s>>>(m, n, groups, c, ldcres, e, f, C, ldc, X_out, t->crt); \
     break;
   switch (t->N) {
     OS2_CASE(1) OS2_CASE(2) OS2_CASE(3) OS2_CASE(4) OS2_CASE(5) OS2_CASE(6) OS2_CASE(7)

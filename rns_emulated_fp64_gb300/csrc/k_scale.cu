@@ -20,8 +20,8 @@
 //   k_row_scale  one CTA per row: exponent bound (pass 1), then either the
 //                fast-mode sum of squares and e_i, or the accurate-mode
 //                7-bit magnitude plane (pass 2 re-reads the row from L1/L2).
-//   k_residues   element-parallel: every thread turns 8 consecutive entries
-//                into 8 residues per modulus and writes one 16-byte vector to
+//   k_residues   element-parallel: every thread turns 4 consecutive entries
+//                into 4 residues per modulus and writes one 8-byte vector to
 //                each plane.  Residues of the odd moduli use FP32 arithmetic
 //                only: the integer is split into 12-bit words w_t and
 //                x = sum_t w_t (2^(12t) mod p) is exact below 2^23, so one
@@ -29,6 +29,8 @@
 //                exactly; mod 256 is the integer's low byte.
 #include <cuda_fp16.h>
 #include <limits.h>
+
+#include <type_traits>
 
 #include "os2_internal.cuh"
 
@@ -255,31 +257,37 @@ __device__ __forceinline__ float byte_residue(uint32_t b) {
   return (float)((int)(b ^ 0x80u) - 128);  // [-128, 127]
 }
 
-template <int N, int NW>
-__device__ __forceinline__ void emit(const float (&w)[8][7], const uint32_t (&lb)[8],
+template <int N, int NW, int EPT>
+__device__ __forceinline__ void emit(const float (&w)[EPT][7], const uint32_t (&lb)[EPT],
                                      const ResConsts &c, __half *dst, size_t pstride) {
+  static_assert(EPT == 4 || EPT == 8, "4 or 8 entries per thread");
+  using Vec = typename std::conditional<EPT == 8, uint4, uint2>::type;
   {
-    __align__(16) __half2 v[4];
+    __align__(16) __half2 v[EPT / 2];
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < EPT / 2; u++)
       v[u] = __floats2half2_rn(byte_residue(lb[2 * u]), byte_residue(lb[2 * u + 1]));
-    *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<uint4 *>(v);
+    *reinterpret_cast<Vec *>(dst) = *reinterpret_cast<Vec *>(v);
   }
 #pragma unroll
   for (int l = 1; l < N; l++) {
-    __align__(16) __half2 v[4];
+    __align__(16) __half2 v[EPT / 2];
 #pragma unroll
-    for (int u = 0; u < 4; u++)
+    for (int u = 0; u < EPT / 2; u++)
       v[u] = __floats2half2_rn(residue_odd<NW>(w[2 * u], c, l),
                                residue_odd<NW>(w[2 * u + 1], c, l));
-    *reinterpret_cast<uint4 *>(dst + l * pstride) = *reinterpret_cast<uint4 *>(v);
+    *reinterpret_cast<Vec *>(dst + l * pstride) = *reinterpret_cast<Vec *>(v);
   }
 }
 
+// Residue planes: EPT consecutive entries per thread, one vector store per plane.
+constexpr int kEPT = 4;
+
 template <int N>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     k_residues(const RowSet a, const RowSet b, int k, int kp, const ResConsts c) {
-  const int cpr = kp / 8;  // 8-entry chunks per row
+  constexpr int EPT = kEPT;
+  const int cpr = kp / EPT;  // chunks per row
   const int total_rows = a.rows + b.rows;
   for (int rr = blockIdx.y; rr < total_rows; rr += gridDim.y) {
     const bool isA = rr < a.rows;
@@ -290,43 +298,43 @@ __global__ void __launch_bounds__(kThreads, 2)
     const size_t pstride = (size_t)rs.rows * kp;
     const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
     for (int ch = blockIdx.x * kThreads + threadIdx.x; ch < cpr; ch += gridDim.x * kThreads) {
-      const int h0 = ch * 8;
-      double v[8];
-      if (vec && h0 + 8 <= k) {
+      const int h0 = ch * EPT;
+      double v[EPT];
+      if (vec && h0 + EPT <= k) {
 #pragma unroll
-        for (int u = 0; u < 4; u++) {
+        for (int u = 0; u < EPT / 2; u++) {
           const double2 t = __ldg(reinterpret_cast<const double2 *>(x + h0) + u);
           v[2 * u] = t.x;
           v[2 * u + 1] = t.y;
         }
       } else {
 #pragma unroll
-        for (int u = 0; u < 8; u++) v[u] = h0 + u < k ? __ldg(x + h0 + u) : 0.0;
+        for (int u = 0; u < EPT; u++) v[u] = h0 + u < k ? __ldg(x + h0 + u) : 0.0;
       }
-      // bit length bound of the 8 integers (row exponent + element exponent)
+      // bit length bound of the integers (row exponent + element exponent)
       int top = INT_MIN;
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
+      for (int u = 0; u < EPT; u++) {
         const uint64_t bits = (uint64_t)__double_as_longlong(v[u]);
         if (bits << 1) top = max(top, max((int)((bits >> 52) & 0x7FF), 1) - 1022 + ee);
       }
-      float w[8][7];
-      uint32_t lb[8];
+      float w[EPT][7];
+      uint32_t lb[EPT];
       __half *dst = rs.planes + (size_t)row * kp + h0;
       if (top <= 60) {
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
+        for (int u = 0; u < EPT; u++) {
           const Dec d = decode(v[u]);
           int_words<5>(d, d.ex2 + ee, w[u], lb[u]);
         }
-        emit<N, 5>(w, lb, c, dst, pstride);
+        emit<N, 5, EPT>(w, lb, c, dst, pstride);
       } else {
 #pragma unroll
-        for (int u = 0; u < 8; u++) {
+        for (int u = 0; u < EPT; u++) {
           const Dec d = decode(v[u]);
           int_words<7>(d, d.ex2 + ee, w[u], lb[u]);
         }
-        emit<N, 7>(w, lb, c, dst, pstride);
+        emit<N, 7, EPT>(w, lb, c, dst, pstride);
       }
     }
   }
@@ -364,7 +372,7 @@ cudaError_t launch_residues(const double *XA, long lda, int rowsA, const int32_t
   if (rowsA + rowsB <= 0 || kp <= 0) return cudaSuccess;
   RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA)};
   RowSet b{XB, ldb, rowsB, const_cast<int32_t *>(eB), nullptr, reinterpret_cast<__half *>(planesB)};
-  const int cpr = kp / 8;
+  const int cpr = kp / kEPT;
   const int bx = (cpr + kThreads - 1) / kThreads;
   const int rows = rowsA + rowsB;
   dim3 grid(bx, rows < 65535 ? rows : 65535);
