@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-context", action="store_true", help="skip native DGEMM / accuracy context")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the N in {14,16,18} x {fast, accurate} sweep of the same workload")
     return ap.parse_args()
 
 
@@ -390,6 +392,31 @@ def run_ours(a):
                                 "gpu_result_bit_exact_on_sample": same}
         if not same:
             line["parity_error"] = int(np.count_nonzero(got != ref.C))
+
+    # the rest of the 8192^3 configuration: N in {14, 16, 18}, both modes
+    if not a.no_sweep:
+        sweep = {}
+        for Ns in (14, 16, 18):
+            for mode in ("fast", "accurate"):
+                wss = os2.alloc_workspace(os2.workspace_size(m, n, k, Ns, mode), dev)
+                Cs = torch.empty((m, n), dtype=torch.float64, device=dev)
+                for _ in range(2):
+                    os2.gemm(Ad, Bd, Ns, mode, out=Cs, workspace=wss, stream=stream)
+                torch.cuda.synchronize(dev)
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                reps = 10
+                s0.record(stream)
+                for _ in range(reps):
+                    os2.gemm(Ad, Bd, Ns, mode, out=Cs, workspace=wss, stream=stream)
+                s1.record(stream)
+                torch.cuda.synchronize(dev)
+                if os2.get_status(stream):
+                    raise RuntimeError("device status set during the sweep")
+                sms = s0.elapsed_time(s1) / reps
+                sweep[f"N{Ns}_{mode}"] = {"ms": sms, "tflops": flop / (sms / 1e3) / 1e12}
+                del wss, Cs
+                torch.cuda.empty_cache()
+        line["sweep_8192cube"] = sweep
 
     # context: native cuBLAS DGEMM rate and accuracy against the exact product
     if rank == 0 and not a.no_context:
