@@ -29,8 +29,12 @@
  *    256,255,253,251,247,241,239,233,229,227,223,217,211,199,197,193,191,181,179,173
  *    ([Q] "256以下の法の選び方(手順2)", footnote 6).  14-16 give about
  *    native-FP64 accuracy ([Q] "行列積の回数と性能").
- *  - 0 <= k < 131072 (2^17): the bound that keeps residue products exact in
- *    INT32 ([Q] "誤差のないINT8行列積(手順3)").
+ *  - 0 <= k < 2^24.  [Q] "誤差のないINT8行列積(手順3)": INT32 sums of residue
+ *    products are exact only while k < 2^17, and larger k is split into
+ *    blocks.  Here step 3 reduces every 960-term block mod p_l inside tensor
+ *    memory, so that split is built in and the mod-p products have no such
+ *    limit.  Remaining limits: accurate mode k < 2^19 (its exact int32 bound
+ *    product), raw int32 products from os2_gemm_residues k < 2^17.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every device-side entry point only enqueues work on it and
  *    returns; argument errors are returned synchronously before anything is
@@ -53,7 +57,7 @@ extern "C" {
 typedef enum {
   OS2_OK = 0,
   OS2_ERR_INVALID_ARG = 1,  /* bad size, leading dimension, pointer, mode or N */
-  OS2_ERR_UNSUPPORTED = 2,  /* valid but not supported (k >= 2^17, no GPU support) */
+  OS2_ERR_UNSUPPORTED = 2,  /* valid but beyond a documented size limit */
   OS2_ERR_WORKSPACE = 3,    /* workspace missing or smaller than os2_workspace_size */
   OS2_ERR_NONFINITE = 4,    /* an input entry is Inf or NaN (device-detected) */
   OS2_ERR_RANGE = 5,        /* reserved: CRT bound violated (debug checks) */

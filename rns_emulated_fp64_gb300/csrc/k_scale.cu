@@ -83,22 +83,22 @@ __device__ void shl8(const uint32_t *src, int nsrc, int s, uint32_t *dst) {
     dst[i] = b ? ((cur << b) | (prev >> (32 - b))) : cur;
   }
 }
-__device__ bool fits(uint64_t Q, int g, const uint32_t *H) {
-  uint32_t q2[2] = {(uint32_t)Q, (uint32_t)(Q >> 32)};
+__device__ bool fits(uint64_t Qlo, uint64_t Qhi, int g, const uint32_t *H) {
+  uint32_t q4[4] = {(uint32_t)Qlo, (uint32_t)(Qlo >> 32), (uint32_t)Qhi, (uint32_t)(Qhi >> 32)};
   uint32_t L[8], R[8];
-  shl8(q2, 2, g > 0 ? 2 * g : 0, L);
+  shl8(q4, 4, g > 0 ? 2 * g : 0, L);
   shl8(H, OS2_H_LIMBS, g < 0 ? -2 * g : 0, R);
   for (int i = 7; i >= 0; i--)
     if (L[i] != R[i]) return L[i] < R[i];
   return true;
 }
-// Largest integer g with Q * 4^g <= H, Q >= 1.  With b(.) the bit length,
-// the answer is floor((b(H)+1-b(Q))/2) or one less.
-__device__ int largest_g(uint64_t Q, const ResConsts &c) {
-  int bQ = 64 - __clzll((long long)Q);
+// Largest integer g with Q * 4^g <= H, Q = Qhi 2^64 + Qlo >= 1.  With b(.)
+// the bit length, the answer is floor((b(H)+1-b(Q))/2) or one less.
+__device__ int largest_g(uint64_t Qlo, uint64_t Qhi, const ResConsts &c) {
+  const int bQ = Qhi ? 128 - __clzll((long long)Qhi) : 64 - __clzll((long long)Qlo);
   int g = (c.bitlenH + 1 - bQ) >> 1;
   for (int it = 0; it < 3; it++, g--)
-    if (fits(Q, g, c.H)) return g;
+    if (fits(Qlo, Qhi, g, c.H)) return g;
   return g;
 }
 
@@ -112,16 +112,28 @@ __device__ __forceinline__ int block_max(int v, int *sh) {
   for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
-__device__ __forceinline__ unsigned long long block_sum(unsigned long long v,
-                                                        unsigned long long *sh) {
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+// 128-bit block sum of per-thread 64-bit partials (hi:lo).
+__device__ __forceinline__ void add128(unsigned long long &lo, unsigned long long &hi,
+                                       unsigned long long blo, unsigned long long bhi) {
+  const unsigned long long s = lo + blo;
+  hi += bhi + (s < lo ? 1ull : 0ull);
+  lo = s;
+}
+__device__ __forceinline__ void block_sum128(unsigned long long &lo, unsigned long long &hi,
+                                             unsigned long long *sh) {
+  for (int o = 16; o; o >>= 1)
+    add128(lo, hi, __shfl_xor_sync(0xffffffffu, lo, o), __shfl_xor_sync(0xffffffffu, hi, o));
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
-  if (l == 0) sh[w] = v;
+  if (l == 0) {
+    sh[2 * w] = lo;
+    sh[2 * w + 1] = hi;
+  }
   __syncthreads();
-  v = l < (kThreads / 32) ? sh[l] : 0ull;
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+  lo = l < (kThreads / 32) ? sh[2 * l] : 0ull;
+  hi = l < (kThreads / 32) ? sh[2 * l + 1] : 0ull;
+  for (int o = 16; o; o >>= 1)
+    add128(lo, hi, __shfl_xor_sync(0xffffffffu, lo, o), __shfl_xor_sync(0xffffffffu, hi, o));
 }
 
 __device__ __forceinline__ void set_status(int *status, int code) {
@@ -142,7 +154,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads)
     k_row_scale(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
   __shared__ int s_int[32];
-  __shared__ unsigned long long s_u64[32];
+  __shared__ unsigned long long s_u64[2 * 32];
   const bool isA = (int)blockIdx.x < a.rows;
   const RowSet &rs = isA ? a : b;
   const int row = isA ? (int)blockIdx.x : (int)blockIdx.x - a.rows;
@@ -196,14 +208,17 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // pass 2 (fast mode): exact sum of squares of the 23-bit upper roundings
-  unsigned long long Q = 0;
+  // (each q^2 <= 2^46; a thread's partial stays below 2^64 for k < 2^26;
+  // the block sum is 128-bit)
+  unsigned long long Q = 0, Qhi = 0;
   for (int h = threadIdx.x; h < k; h += kThreads) {
     const Dec d = decode(__ldg(x + h));
     const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
     Q += q * q;
   }
-  Q = block_sum(Q, s_u64);
-  if (threadIdx.x == 0) rs.e[row] = (nonzero && !bad && Q) ? largest_g(Q, c) + 23 - E : 0;
+  block_sum128(Q, Qhi, s_u64);
+  if (threadIdx.x == 0)
+    rs.e[row] = (nonzero && !bad && (Q | Qhi)) ? largest_g(Q, Qhi, c) + 23 - E : 0;
 }
 
 // --------------------------------------------------------------- residues --
@@ -345,7 +360,7 @@ __global__ void k_accu_exponents(const int32_t *__restrict__ bound, const int32_
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows) return;
   int R = bound[i];
-  e[i] = R > 0 ? largest_g((uint64_t)R, c) + 6 - E[i] : -E[i];
+  e[i] = R > 0 ? largest_g((uint64_t)R, 0ull, c) + 6 - E[i] : -E[i];
 }
 
 }  // namespace

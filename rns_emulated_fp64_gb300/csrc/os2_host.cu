@@ -215,7 +215,14 @@ const Os2Tables *os2_tables(int N) {
 // ---------------------------------------------------------------------------
 namespace {
 
-constexpr int kMaxK = 1 << 17;
+// Inner-dimension limits.  Step 3 reduces every 960-term block mod p inside
+// tensor memory, so the mod-p path has no INT32 limit; the remaining limits
+// are the fast-mode sums (exact for k < 2^26 per thread partial, kept well
+// inside), the accurate-mode bound product (int32 sums of 64*64*k < 2^31) and
+// raw int32 products (128*128*k < 2^31).
+constexpr int kMaxK = 1 << 24;
+constexpr int kMaxKAccurate = 1 << 19;
+constexpr int kMaxKRaw = 1 << 17;
 
 struct Layout {
   size_t e, f, EA, EB, R, K, planesA, planesB, cres, total;
@@ -266,7 +273,7 @@ os2_status check_gemm_args(int m, int n, int k, const double *A, int lda, const 
   if (mode != OS2_MODE_FAST && mode != OS2_MODE_ACCURATE) return OS2_ERR_INVALID_ARG;
   if (lda < std::max(k, 1) || ldb < std::max(k, 1) || ldc < std::max(n, 1))
     return OS2_ERR_INVALID_ARG;
-  if (k >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if (k >= kMaxK || (mode == OS2_MODE_ACCURATE && k >= kMaxKAccurate)) return OS2_ERR_UNSUPPORTED;
   if (m > 0 && n > 0 && !C) return OS2_ERR_INVALID_ARG;
   if (m > 0 && k > 0 && !A) return OS2_ERR_INVALID_ARG;
   if (n > 0 && k > 0 && !B) return OS2_ERR_INVALID_ARG;
@@ -410,6 +417,7 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
   if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
   if (mode != OS2_MODE_FAST && mode != OS2_MODE_ACCURATE) return OS2_ERR_INVALID_ARG;
   if (k >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if (mode == OS2_MODE_ACCURATE && k >= kMaxKAccurate) return OS2_ERR_UNSUPPORTED;
   if ((m && (!e || (k && !A))) || (n && (!f || (k && !B)))) return OS2_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Os2Tables *t = os2_tables(num_moduli);
@@ -468,7 +476,7 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
   if (ldo < std::max(n, 1)) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_MODP_INT8 && ldo % OS2_CRES_ALIGN) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_RAW_INT32 && ldo % 4) return OS2_ERR_INVALID_ARG;
-  if (ldp >= kMaxK) return OS2_ERR_UNSUPPORTED;
+  if (ldp >= kMaxK || (out_kind == OS2_OUT_RAW_INT32 && k >= kMaxKRaw)) return OS2_ERR_UNSUPPORTED;
   if (m == 0 || n == 0) return OS2_OK;
   if (!out || !aligned(out, 16)) return OS2_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -72,7 +72,9 @@ def test_argument_errors_are_synchronous():
     assert g(4, 4, 4, P, 4, P, 4, P, 4, 21, 0, None, 0, None) == binding.ERR_INVALID_ARG
     assert g(4, 4, 4, P, 4, P, 4, P, 4, 14, 2, None, 0, None) == binding.ERR_INVALID_ARG   # mode
     assert g(4, 4, 4, None, 4, P, 4, P, 4, 14, 0, None, 0, None) == binding.ERR_INVALID_ARG
-    assert g(4, 4, 1 << 17, P, 1 << 17, P, 1 << 17, P, 4, 14, 0, None, 0, None) == binding.ERR_UNSUPPORTED
+    assert g(4, 4, 1 << 24, P, 1 << 24, P, 1 << 24, P, 4, 14, 0, None, 0, None) == binding.ERR_UNSUPPORTED
+    assert g(4, 4, 1 << 19, P, 1 << 19, P, 1 << 19, P, 4, 14, 1, None, 0, None) == binding.ERR_UNSUPPORTED
+    assert g(4, 4, 1 << 19, P, 1 << 19, P, 1 << 19, P, 4, 14, 0, None, 0, None) == binding.ERR_WORKSPACE
     assert g(4, 4, 4, P, 4, P, 4, P, 4, 14, 0, None, 0, None) == binding.ERR_WORKSPACE
     assert g(4, 4, 4, P, 4, P, 4, P, 4, 14, 0, ct.c_void_p(0x1001), 1 << 20, None) == binding.ERR_WORKSPACE
     assert g(4, 4, 4, ct.c_void_p(0x1004), 4, P, 4, P, 4, 14, 0, None, 0, None) == binding.ERR_INVALID_ARG
@@ -83,6 +85,8 @@ def test_argument_errors_are_synchronous():
     assert gr(4, 4, 4, P, P, 64, 14, 0, P, 8, 0, None) == binding.ERR_INVALID_ARG   # ldo % 16 for int8
     assert gr(4, 4, 4, P, P, 64, 14, 2, P, 16, 0, None) == binding.ERR_INVALID_ARG  # out kind
     assert gr(4, 4, 4, P, P, 64, 14, 0, P, 16, 5, None) == binding.ERR_INVALID_ARG  # variant
+    big = 1 << 17
+    assert gr(4, 4, big, P, P, big, 14, 1, P, 4, 0, None) == binding.ERR_UNSUPPORTED  # raw int32 k limit
     c = lib.os2_crt
     assert c(4, 4, P, 2, 14, P, P, P, 4, None, None) == binding.ERR_INVALID_ARG     # ldcres < n
     assert lib.os2_set_gemm_variant(3) == binding.ERR_INVALID_ARG

@@ -334,3 +334,52 @@ def test_host_entry_point_matches_device():
     status_ok()
     Cd = os2.gemm(dev(A), dev(Bt), 14).cpu().numpy()
     assert_bits_equal(Ch.numpy(), Cd, "host vs device entry")
+
+
+# ----------------------------------------------------- inner dimension >= 2^17 --
+@pytest.mark.parametrize("N,m,n,k", [(16, 24, 20, 140001), (20, 8, 9, 300000), (12, 130, 5, 131073)])
+def test_large_k_fast_parity(N, m, n, k):
+    """[Q] 手順3: beyond 2^17 the products are split into blocks; here every
+    960-term block is reduced mod p in tensor memory, so k may exceed 2^17."""
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=k % 97, phi=1.0)
+    C = os2.gemm(dev(A), dev(Bt), N, "fast").cpu().numpy()
+    status_ok()
+    ref = orc.gemm_entries(A, Bt, N, want_X=False, want_c=False, want_G=False)
+    assert ref.mismatches == 0
+    assert_bits_equal(C, ref.C, f"k={k}")
+
+
+def test_large_k_accurate_parity():
+    A, Bt = workloads.make_pair("spread", 10, 12, 200003, seed=3, phi=2.0)
+    C = os2.gemm(dev(A), dev(Bt), 16, "accurate").cpu().numpy()
+    status_ok()
+    ref = orc.gemm_entries(A, Bt, 16, mode=orc.ACCURATE, want_X=False, want_c=False, want_G=False)
+    assert_bits_equal(C, ref.C, "accurate, k=200003")
+
+
+def test_large_k_all_ones_128bit_sums():
+    """All-ones rows with k > 2^20: the fast-mode sum of squares exceeds 2^64
+    (128-bit path); C = k exactly and the exponents match the oracle."""
+    k = (1 << 20) + 5
+    A = np.ones((4, k))
+    Bt = np.ones((3, k))
+    e, f = os2.scale(dev(A), dev(Bt), 16, "fast")
+    assert np.array_equal(e.cpu().numpy(), orc.scale_fast(A, 16))
+    C = os2.gemm(dev(A), dev(Bt), 16, "fast")
+    status_ok()
+    assert torch.all(C == k)
+
+
+def test_modp_products_far_beyond_int32():
+    """All residues -128 with k = 2^20: G = 2^14 k overflows int32, but the
+    blocked mod-p accumulation gives (2^14 k) mod p exactly."""
+    N, m, n, k = 5, 128, 256, 1 << 20
+    RA = torch.full((N, m, k), -128.0, dtype=torch.float16, device=DEV)
+    RB = torch.full((N, n, k), -128.0, dtype=torch.float16, device=DEV)
+    for variant in (os2.GEMM_TC, os2.GEMM_TC_1SM):
+        c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, variant).cpu().numpy()[:, :, :n]
+        status_ok()
+        for l, p in enumerate(os2.moduli(N)):
+            r = (16384 * k) % p
+            r = r - p if r >= (p + 1) // 2 else r
+            assert np.all(c[l] == r), (variant, p)
