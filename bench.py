@@ -417,6 +417,23 @@ def run_ours(a):
                 del wss, Cs
                 torch.cuda.empty_cache()
         line["sweep_8192cube"] = sweep
+        # SGEMM emulation of the same workload (float32 operands, binary32 result)
+        Af, Bf = Ad.float(), Bd.float()
+        Cf = torch.empty((m, n), dtype=torch.float32, device=dev)
+        wsf = os2.alloc_workspace(os2.workspace_size(m, n, k, 7, "fast"), dev)
+        for _ in range(2):
+            os2.sgemm(Af, Bf, 7, "fast", out=Cf, workspace=wsf, stream=stream)
+        torch.cuda.synchronize(dev)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(10):
+            os2.sgemm(Af, Bf, 7, "fast", out=Cf, workspace=wsf, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        sms = s0.elapsed_time(s1) / 10
+        line["sgemm_8192cube_N7_fast"] = {"ms": sms, "tflops": flop / (sms / 1e3) / 1e12}
+        del Af, Bf, Cf, wsf
+        torch.cuda.empty_cache()
 
     # context: native cuBLAS DGEMM rate and accuracy against the exact product
     if rank == 0 and not a.no_context:

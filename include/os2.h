@@ -93,6 +93,18 @@ os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double 
                     double *C, int ldc, int num_moduli, int mode, void *workspace,
                     size_t workspace_bytes, void *stream);
 
+/* SGEMM emulation ([G] "Improved Scaling for Fast Mode of Ozaki Scheme II",
+ * "Ergebnisse": the method is evaluated for DGEMM and SGEMM).  Same five
+ * steps, arguments, layouts, workspace (os2_workspace_size) and errors as
+ * os2_gemm, with float A, B and C: every float is exactly a double, so the
+ * exponents, integers, residues and CRT value are the ones os2_gemm computes
+ * for the same entries; only the final rounding targets binary32 (RN-even,
+ * subnormals, overflow to +-Inf).  Fewer moduli suffice (about 7 for FP32
+ * accuracy at k ~ 10^3-10^4). */
+os2_status os2_sgemm(int m, int n, int k, const float *A, int lda, const float *B, int ldb,
+                     float *C, int ldc, int num_moduli, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
 /* Device workspace for os2_gemm_host: os2_workspace_size plus device copies
  * of A (m*k), B (k*n) and C (m*n) doubles. */
 size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode);

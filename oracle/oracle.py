@@ -63,6 +63,9 @@ def load():
             lib.orc_residues.argtypes = [i32, i32, P, l, P, i32, P]
             lib.orc_round_scaled.argtypes = [P, i32]
             lib.orc_round_scaled.restype = ct.c_double
+            lib.orc_round_scaled_f32.argtypes = [P, i32]
+            lib.orc_round_scaled_f32.restype = ct.c_double
+            lib.orc_set_output_f32.argtypes = [i32]
             lib.orc_gemm_entries.argtypes = [i32, i32, i32, P, l, P, l, i32, i32, P, i32, P,
                                              i32, P, P, P, P, P, P, P]
             lib.orc_num_threads.restype = i32
@@ -149,6 +152,11 @@ def round_scaled(X: int, s: int) -> float:
     return float(load().orc_round_scaled(_ptr(int_to_limbs(X)), s))
 
 
+def round_scaled_f32(X: int, s: int) -> float:
+    """RN-even of X * 2^-s to binary32 (value returned as a Python float)."""
+    return float(load().orc_round_scaled_f32(_ptr(int_to_limbs(X)), s))
+
+
 # --------------------------------------------------------------------------
 # steps
 # --------------------------------------------------------------------------
@@ -216,13 +224,16 @@ class Entries:
 
 
 def gemm_entries(A, Bt, N: int, rows=None, cols=None, mode: int = FAST, e=None, f=None,
-                 want_X=True, want_c=True, want_G=True) -> Entries:
+                 want_X=True, want_c=True, want_G=True, out_f32=False) -> Entries:
     """Steps 1-5 for the output entries rows x cols.
 
     In FAST mode the exponents are computed from the selected rows/columns
     alone.  In ACCURATE mode they come from ``scale_accu`` (or are passed in
-    as e, f for the selected rows/columns).
+    as e, f for the selected rows/columns).  float32 inputs are taken as the
+    doubles they equal; out_f32 rounds C to binary32 (SGEMM emulation).
     """
+    A = np.ascontiguousarray(A, dtype=np.float64) if np.asarray(A).dtype == np.float32 else A
+    Bt = np.ascontiguousarray(Bt, dtype=np.float64) if np.asarray(Bt).dtype == np.float32 else Bt
     A, lda = _rows(A)
     Bt, ldb = _rows(Bt)
     m, k = A.shape
@@ -245,9 +256,17 @@ def gemm_entries(A, Bt, N: int, rows=None, cols=None, mode: int = FAST, e=None, 
     c = np.zeros((nr, nc, N), np.int8) if want_c else None
     G = np.zeros((nr, nc, N), np.int64) if want_G else None
     bad = np.zeros(1, np.int64)
-    _check(load().orc_gemm_entries(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, N, nr, _ptr(rows), nc,
-                                   _ptr(cols), compute, _ptr(e), _ptr(f), _ptr(C), _ptr(X),
-                                   _ptr(c), _ptr(G), _ptr(bad)), "orc_gemm_entries")
+    lib = load()
+    with _lock:
+        lib.orc_set_output_f32(1 if out_f32 else 0)
+        try:
+            _check(lib.orc_gemm_entries(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, N, nr, _ptr(rows),
+                                        nc, _ptr(cols), compute, _ptr(e), _ptr(f), _ptr(C), _ptr(X),
+                                        _ptr(c), _ptr(G), _ptr(bad)), "orc_gemm_entries")
+        finally:
+            lib.orc_set_output_f32(0)
+    if out_f32:
+        C = C.astype(np.float32)
     return Entries(rows=rows, cols=cols, e=e, f=f, C=C, X=X, c=c, G=G, mismatches=int(bad[0]))
 
 

@@ -470,16 +470,20 @@ int orc_residues(int rows, int k, const double *X, long ldx, const int32_t *e, i
 /* Step 5 -- one correctly rounded conversion of X * 2^-s to binary64         */
 /* ------------------------------------------------------------------------- */
 
-/* Round-to-nearest-even of X * 2^(-s), subnormals and overflow included.
- * Keeps the bits of |X| at positions >= cut, where cut is the larger of
- * bitlen - 53 (53-bit significand) and s - 1074 (weight 2^-1074). */
-static double round_scaled(big_t X, int s) {
+/* Round-to-nearest-even of X * 2^(-s) to a binary format with a prec-bit
+ * significand and minimum normal exponent emin (binary64: 53, -1022;
+ * binary32: 24, -126), subnormals and overflow included.  Keeps the bits of
+ * |X| at positions >= cut, where cut is the larger of bitlen - prec and
+ * s - (prec - 1 - emin) (the weight of the smallest subnormal).  The result is
+ * returned as a double holding the value of that format (+-Inf on overflow). */
+static double round_scaled_fmt(big_t X, int s, int prec, int emin, int emax) {
+  const int lsb = prec - 1 - emin;
   int neg = big_is_neg(&X);
   big_t M = neg ? big_neg(X) : X;
   if (big_is_zero(&M)) return 0.0;
   int b = big_bitlen(M);
-  int cut = b - 53;
-  if (s - 1074 > cut) cut = s - 1074;
+  int cut = b - prec;
+  if (s - lsb > cut) cut = s - lsb;
   uint64_t kept;
   if (cut <= 0) {
     kept = (uint64_t)M.w[0] | ((uint64_t)M.w[1] << 32);   /* exact: M < 2^53 */
@@ -495,11 +499,22 @@ static double round_scaled(big_t X, int s) {
   }
   if (cut < 0) cut = 0;
   double r = ldexp((double)kept, cut - s);
+  if (r >= ldexp(1.0, emax + 1)) r = INFINITY;  /* rounded value beyond the format */
   return neg ? -r : r;
 }
 
+static double round_scaled(big_t X, int s) { return round_scaled_fmt(X, s, 53, -1022, 1023); }
+
 /* exported for the rounding pins: X given as 8 u32 limbs (two's complement) */
 double orc_round_scaled(const uint32_t *X, int s) { return round_scaled(big_in(X), s); }
+double orc_round_scaled_f32(const uint32_t *X, int s) {
+  return round_scaled_fmt(big_in(X), s, 24, -126, 127);
+}
+
+/* Output format of orc_gemm_entries: binary64 (DGEMM) or binary32 (SGEMM;
+ * [G] "Ergebnisse": the revised scaling is evaluated for SGEMM too). */
+static int orc_out_f32 = 0;
+void orc_set_output_f32(int on) { orc_out_f32 = on ? 1 : 0; }
 
 /* ------------------------------------------------------------------------- */
 /* Steps 3-5 for selected output entries                                      */
@@ -586,7 +601,8 @@ int orc_gemm_entries(int m, int n, int k, const double *A, long lda, const doubl
       if (big_cmp(Xc, t.half) >= 0) Xc = big_sub(Xc, t.P); /* lift [P/2, P) to [-P/2, 0) */
       if (big_cmp(Xc, Xd) != 0) bad++;
       if (X) big_out(Xc, X + idx * NL);
-      if (C) C[idx] = round_scaled(Xc, e_rows[a] + f_cols[b]);
+      if (C) C[idx] = orc_out_f32 ? round_scaled_fmt(Xc, e_rows[a] + f_cols[b], 24, -126, 127)
+                                  : round_scaled(Xc, e_rows[a] + f_cols[b]);
     }
   }
   free(Ai); free(Bi); free(rA); free(rB);

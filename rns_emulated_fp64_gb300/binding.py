@@ -26,7 +26,7 @@ EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gem
            "os2_scale", "os2_residues", "os2_gemm_residues", "os2_crt", "os2_moduli",
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
            "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
-           "os2_gemm_noalloc")
+           "os2_gemm_noalloc", "os2_sgemm")
 
 _lib = None
 _lock = threading.Lock()
@@ -87,6 +87,8 @@ def load(build_if_missing: bool = True):
         L.os2_profile_stop.restype = i
         L.os2_gemm_noalloc.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp]
         L.os2_gemm_noalloc.restype = i
+        L.os2_sgemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
+        L.os2_sgemm.restype = i
         _lib = L
         return L
 
@@ -177,6 +179,29 @@ def gemm(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 14, mode="fast", o
     st = load().os2_gemm(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, _ptr(out), ldc, num_moduli,
                          _mode(mode), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "os2_gemm")
+    return out
+
+
+def sgemm(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 7, mode="fast", out=None,
+          workspace=None, stream=None) -> torch.Tensor:
+    """C = A @ Bt.T for float32 operands (SGEMM emulation); layouts as in gemm."""
+    for X, nm in ((A, "A"), (Bt, "Bt")):
+        if not (X.is_cuda and X.dtype == torch.float32 and X.dim() == 2 and X.stride(1) == 1):
+            raise ValueError(f"{nm} must be a 2-D float32 CUDA tensor with contiguous rows")
+    m, k = A.shape
+    n = Bt.shape[0]
+    if Bt.shape[1] != k:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32, device=A.device)
+    need = workspace_size(m, n, k, num_moduli, mode)
+    if workspace is None:
+        workspace = alloc_workspace(need, A.device)
+    st = load().os2_sgemm(m, n, k, _ptr(A), max(A.stride(0), max(k, 1)), _ptr(Bt),
+                          max(Bt.stride(0), max(k, 1)), _ptr(out), max(out.stride(0), max(n, 1)),
+                          num_moduli, _mode(mode), _ptr(workspace), workspace.numel(),
+                          _stream(stream))
+    _check(st, "os2_sgemm")
     return out
 
 

@@ -32,21 +32,50 @@ struct Limbs {
   static constexpr int LX = LW + 1;
 };
 
-// RN-even of |X| * 2^-s with |X| in 32-bit limbs m[0..L), sign `neg`
-// (general routine: zero, subnormal and overflowing results; kept out of line).
-template <int L>
-__device__ __noinline__ double round_scaled(const uint32_t (&m)[L], bool neg, int s) {
+// Target formats: binary64 (DGEMM) and binary32 (SGEMM emulation).
+template <typename OutT>
+struct Fmt;
+template <>
+struct Fmt<double> {
+  static constexpr int prec = 53, emin = -1022, emax = 1023;
+  static __device__ __forceinline__ double make(uint64_t mant, int ex, bool neg, int kind) {
+    // kind 0: normal (mant has prec bits, ex unbiased); 1: subnormal bits in mant; 2: inf
+    uint64_t b = kind == 2 ? 0x7FF0000000000000ull
+                           : (kind == 1 ? mant : (((uint64_t)(ex + 1023) << 52) | (mant & ((1ull << 52) - 1))));
+    if (neg) b |= 1ull << 63;
+    return __longlong_as_double((long long)b);
+  }
+};
+template <>
+struct Fmt<float> {
+  static constexpr int prec = 24, emin = -126, emax = 127;
+  static __device__ __forceinline__ float make(uint64_t mant, int ex, bool neg, int kind) {
+    uint32_t b = kind == 2 ? 0x7F800000u
+                           : (kind == 1 ? (uint32_t)mant
+                                        : (((uint32_t)(ex + 127) << 23) | ((uint32_t)mant & 0x7FFFFFu)));
+    if (neg) b |= 1u << 31;
+    return __uint_as_float(b);
+  }
+};
+
+// RN-even of |X| * 2^-s to the format of OutT, |X| in 32-bit limbs m[0..L),
+// sign `neg` (general routine: zero, subnormal and overflowing results; kept
+// out of line).
+template <typename OutT, int L>
+__device__ __noinline__ OutT round_scaled(const uint32_t (&m)[L], bool neg, int s) {
+  using F = Fmt<OutT>;
+  constexpr int lsb = F::prec - 1 - F::emin;  // -log2 of the smallest subnormal
   int top = -1;
 #pragma unroll
   for (int u = 0; u < L; u++)
     if (m[u]) top = u;
-  if (top < 0) return 0.0;
+  if (top < 0) return OutT(0);
   uint32_t mt = 0;
 #pragma unroll
   for (int u = 0; u < L; u++)
     if (u == top) mt = m[u];
   const int b = 32 * top + 32 - __clz(mt);  // bit length of |X|
-  int cut = max(b - 53, s - 1074);
+  int cut = max(b - F::prec, s - lsb);
   uint64_t kept;
   if (cut <= 0) {
     kept = (uint64_t)m[0] | (L > 1 ? (uint64_t)m[L > 1 ? 1 : 0] << 32 : 0ull);
@@ -54,7 +83,7 @@ __device__ __noinline__ double round_scaled(const uint32_t (&m)[L], bool neg, in
   } else if (cut > b) {
     kept = 0;
   } else {
-    // bits [cut, cut + 54) of |X|, round bit cut - 1, sticky below
+    // bits [cut, cut + prec + 1) of |X|, round bit cut - 1, sticky below
     const int w = cut >> 5, o = cut & 31;
     uint32_t a0 = 0, a1 = 0, a2 = 0;
 #pragma unroll
@@ -78,32 +107,25 @@ __device__ __noinline__ double round_scaled(const uint32_t (&m)[L], bool neg, in
     sticky |= (rwv & ((1u << ro) - 1u)) != 0;
     if (round && (sticky || (kept & 1))) kept++;
   }
-  if (kept == 0) return neg ? -0.0 : 0.0;
+  if (kept == 0) return neg ? -OutT(0) : OutT(0);
   const int x = cut - s;  // value = kept * 2^x
   const int bk = 64 - __clzll((long long)kept);
   const int etop = x + bk - 1;
-  uint64_t bits;
-  if (etop >= -1022) {
-    if (etop > 1023) {
-      bits = 0x7FF0000000000000ull;
-    } else {
-      const uint64_t mant = bk >= 53 ? kept >> (bk - 53) : kept << (53 - bk);
-      bits = ((uint64_t)(etop + 1023) << 52) | (mant & ((1ull << 52) - 1));
-    }
-  } else {
-    bits = kept << (x + 1074);  // subnormal: x >= -1074 by construction of cut
+  if (etop >= F::emin) {
+    if (etop > F::emax) return F::make(0, 0, neg, 2);
+    const uint64_t mant = bk >= F::prec ? kept >> (bk - F::prec) : kept << (F::prec - bk);
+    return F::make(mant, etop, neg, 0);
   }
-  if (neg) bits |= 1ull << 63;
-  return __longlong_as_double((long long)bits);
+  return F::make(kept << (x + lsb), 0, neg, 1);  // subnormal: x >= -lsb by construction of cut
 }
 
-
-// Normal-range fast path of round_scaled: the top three nonzero-anchored limbs
-// hold at least 65 significant bits, enough for 53 bits, the round bit and a
-// sticky bit (OR-ed with everything below).  Falls back to the general routine
-// for zero, subnormal or overflowing results.
-template <int L>
-__device__ __forceinline__ double round_scaled_fast(const uint32_t (&m)[L], bool neg, int s) {
+// Normal-range fast path: the top three nonzero-anchored limbs hold at least
+// 65 significant bits, enough for the significand, the round bit and a sticky
+// bit (OR-ed with everything below).  Falls back to the general routine for
+// zero, subnormal or overflowing results.
+template <typename OutT, int L>
+__device__ __forceinline__ OutT round_scaled_fast(const uint32_t (&m)[L], bool neg, int s) {
+  using F = Fmt<OutT>;
   int t = -1;
 #pragma unroll
   for (int u = 0; u < L; u++)
@@ -119,32 +141,29 @@ __device__ __forceinline__ double round_scaled_fast(const uint32_t (&m)[L], bool
   }
   const int lz = __clz(hi);
   const int etop = 32 * t + 31 - lz - s;  // exponent of the leading bit of |X| 2^-s
-  if (t < 0 || etop < -1022 || etop > 1023) return round_scaled<L>(m, neg, s);
+  if (t < 0 || etop < F::emin || etop > F::emax) return round_scaled<OutT, L>(m, neg, s);
   const uint32_t t1 = __funnelshift_l(mid, hi, lz);
   const uint32_t t0 = __funnelshift_l(lo, mid, lz);
   const uint32_t tail = lo << lz;  // bits below the 64-bit window (lz < 32)
   const uint64_t T = ((uint64_t)t1 << 32) | t0;
-  uint64_t kept = T >> 11;  // 53 bits, leading bit set
-  const bool round = (T >> 10) & 1;
-  const bool sticky = (T & 0x3FFull) != 0 || tail != 0 || rest;
+  uint64_t kept = T >> (64 - F::prec);  // leading bit set
+  const bool round = (T >> (63 - F::prec)) & 1;
+  const bool sticky = (T & ((1ull << (63 - F::prec)) - 1)) != 0 || tail != 0 || rest;
   int ex = etop;
   if (round && (sticky || (kept & 1))) {
     kept++;
-    if (kept >> 53) {
+    if (kept >> F::prec) {
       kept >>= 1;
       ex++;
     }
   }
-  uint64_t bits = ex > 1023 ? 0x7FF0000000000000ull
-                            : (((uint64_t)(ex + 1023) << 52) | (kept & ((1ull << 52) - 1)));
-  if (neg) bits |= 1ull << 63;
-  return __longlong_as_double((long long)bits);
+  return ex > F::emax ? F::make(0, 0, neg, 2) : F::make(kept, ex, neg, 0);
 }
 
-template <int N>
+template <int N, typename OutT>
 __global__ void __launch_bounds__(kThreads)
     k_crt(int m, int n, int groups, const int8_t *__restrict__ c, int ldcres,
-          const int32_t *__restrict__ e, const int32_t *__restrict__ f, double *__restrict__ C,
+          const int32_t *__restrict__ e, const int32_t *__restrict__ f, OutT *__restrict__ C,
           int ldc, uint32_t *__restrict__ Xout, const CrtConsts cc) {
   constexpr int LW = Limbs<N>::LW, LX = Limbs<N>::LX;
   const int g = blockIdx.x * kThreads + threadIdx.x;
@@ -246,22 +265,19 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int v = 0; v < LX; v++) mag[v] = x[v];
     }
-    C[(size_t)i * ldc + j] = round_scaled_fast<LX>(mag, neg, ei + f[j]);
+    C[(size_t)i * ldc + j] = round_scaled_fast<OutT, LX>(mag, neg, ei + f[j]);
   }
   }
 }
 
-}  // namespace
-
-cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t *e,
-                       const int32_t *f, double *C, int ldc, uint32_t *X_out, const Os2Tables *t,
-                       cudaStream_t s) {
-  if (m <= 0 || n <= 0) return cudaSuccess;
+template <typename OutT>
+cudaError_t crt_t(int m, int n, const int8_t *c, int ldcres, const int32_t *e, const int32_t *f,
+                  OutT *C, int ldc, uint32_t *X_out, const Os2Tables *t, cudaStream_t s) {
   const int groups = (n + 3) / 4;
   const dim3 grid((groups + kThreads - 1) / kThreads, m < 65535 ? m : 65535);
-#define OS2_CASE(NN)                                                                       \
-  case NN:                                                                                 \
-    k_crt<NN><<<grid, kThreads, 0, s>>>(m, n, groups, c, ldcres, e, f, C, ldc, X_out, t->crt); \
+#define OS2_CASE(NN)                                                                              \
+  case NN:                                                                                        \
+    k_crt<NN, OutT><<<grid, kThreads, 0, s>>>(m, n, groups, c, ldcres, e, f, C, ldc, X_out, t->crt); \
     break;
   switch (t->N) {
     OS2_CASE(1) OS2_CASE(2) OS2_CASE(3) OS2_CASE(4) OS2_CASE(5) OS2_CASE(6) OS2_CASE(7)
@@ -271,4 +287,14 @@ cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t 
   }
 #undef OS2_CASE
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_crt(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
+                       const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
+                       cudaStream_t s) {
+  if (m <= 0 || n <= 0) return cudaSuccess;
+  return f32 ? crt_t<float>(m, n, c, ldcres, e, f, static_cast<float *>(C), ldc, X_out, t, s)
+             : crt_t<double>(m, n, c, ldcres, e, f, static_cast<double *>(C), ldc, X_out, t, s);
 }

@@ -59,6 +59,32 @@ __device__ __forceinline__ Dec decode(double x) {
   return d;
 }
 
+__device__ __forceinline__ Dec decode(float x) {
+  const uint32_t b = __float_as_uint(x);
+  int bexp = (int)((b >> 23) & 0xFF);
+  Dec d;
+  d.neg = b >> 31;
+  d.nonfinite = bexp == 0xFF;
+  d.mant = b & 0x7FFFFFu;
+  if (bexp) d.mant |= 1ull << 23;
+  else bexp = 1;
+  d.ex2 = bexp - 150;
+  if (d.nonfinite) d.mant = 0;
+  return d;
+}
+
+// Two consecutive entries through one vector load (aligned to 2 * sizeof(T)).
+__device__ __forceinline__ void load2(const double *p, double &a, double &b) {
+  const double2 v = __ldg(reinterpret_cast<const double2 *>(p));
+  a = v.x;
+  b = v.y;
+}
+__device__ __forceinline__ void load2(const float *p, float &a, float &b) {
+  const float2 v = __ldg(reinterpret_cast<const float2 *>(p));
+  a = v.x;
+  b = v.y;
+}
+
 // Tight E with |x| < 2^E; INT_MIN for zero.
 __device__ __forceinline__ int exp_bound(const Dec &d) {
   return d.mant ? d.ex2 + (64 - __clzll((long long)d.mant)) : INT_MIN;
@@ -141,7 +167,7 @@ __device__ __forceinline__ void set_status(int *status, int code) {
 }
 
 struct RowSet {
-  const double *X;
+  const void *X;    // double or float entries, row-major
   long ldx;
   int rows;
   int32_t *e;       // exponents (out for scale, in for residues)
@@ -150,7 +176,7 @@ struct RowSet {
 };
 
 // ------------------------------------------------------------- row scale ---
-template <int MODE>
+template <int MODE, typename T>
 __global__ void __launch_bounds__(kThreads)
     k_row_scale(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
   __shared__ int s_int[32];
@@ -158,16 +184,17 @@ __global__ void __launch_bounds__(kThreads)
   const bool isA = (int)blockIdx.x < a.rows;
   const RowSet &rs = isA ? a : b;
   const int row = isA ? (int)blockIdx.x : (int)blockIdx.x - a.rows;
-  const double *x = rs.X + (size_t)row * rs.ldx;
-  const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+  const T *x = reinterpret_cast<const T *>(rs.X) + (size_t)row * rs.ldx;
+  const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
 
   // pass 1: exponent bound and finiteness
   int emax = INT_MIN, bad = 0;
   if (vec) {
     for (int h = 2 * threadIdx.x; h < k; h += 2 * kThreads) {
       if (h + 1 < k) {
-        const double2 v = __ldg(reinterpret_cast<const double2 *>(x + h));
-        const Dec d0 = decode(v.x), d1 = decode(v.y);
+        T v0, v1;
+        load2(x + h, v0, v1);
+        const Dec d0 = decode(v0), d1 = decode(v1);
         bad |= d0.nonfinite | d1.nonfinite;
         emax = max(emax, max(exp_bound(d0), exp_bound(d1)));
       } else {
@@ -199,7 +226,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int u = 0; u < 8; u++) {
         const int h = h0 + u;
-        const Dec d = decode(h < k ? __ldg(x + h) : 0.0);
+        const Dec d = decode(h < k ? __ldg(x + h) : T(0));
         v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
       }
       *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
@@ -298,7 +325,7 @@ __device__ __forceinline__ void emit(const float (&w)[EPT][7], const uint32_t (&
 // Residue planes: EPT consecutive entries per thread, one vector store per plane.
 constexpr int kEPT = 4;
 
-template <int N>
+template <int N, typename T>
 __global__ void __launch_bounds__(kThreads, 3)
     k_residues(const RowSet a, const RowSet b, int k, int kp, const ResConsts c) {
   constexpr int EPT = kEPT;
@@ -308,30 +335,26 @@ __global__ void __launch_bounds__(kThreads, 3)
     const bool isA = rr < a.rows;
     const RowSet &rs = isA ? a : b;
     const int row = isA ? rr : rr - a.rows;
-    const double *x = rs.X + (size_t)row * rs.ldx;
+    const T *x = reinterpret_cast<const T *>(rs.X) + (size_t)row * rs.ldx;
     const int ee = __ldg(rs.e + row);
     const size_t pstride = (size_t)rs.rows * kp;
-    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
     for (int ch = blockIdx.x * kThreads + threadIdx.x; ch < cpr; ch += gridDim.x * kThreads) {
       const int h0 = ch * EPT;
-      double v[EPT];
+      T v[EPT];
       if (vec && h0 + EPT <= k) {
 #pragma unroll
-        for (int u = 0; u < EPT / 2; u++) {
-          const double2 t = __ldg(reinterpret_cast<const double2 *>(x + h0) + u);
-          v[2 * u] = t.x;
-          v[2 * u + 1] = t.y;
-        }
+        for (int u = 0; u < EPT / 2; u++) load2(x + h0 + 2 * u, v[2 * u], v[2 * u + 1]);
       } else {
 #pragma unroll
-        for (int u = 0; u < EPT; u++) v[u] = h0 + u < k ? __ldg(x + h0 + u) : 0.0;
+        for (int u = 0; u < EPT; u++) v[u] = h0 + u < k ? __ldg(x + h0 + u) : T(0);
       }
       // bit length bound of the integers (row exponent + element exponent)
       int top = INT_MIN;
 #pragma unroll
       for (int u = 0; u < EPT; u++) {
-        const uint64_t bits = (uint64_t)__double_as_longlong(v[u]);
-        if (bits << 1) top = max(top, max((int)((bits >> 52) & 0x7FF), 1) - 1022 + ee);
+        const Dec d = decode(v[u]);
+        if (d.mant) top = max(top, d.ex2 + 64 - __clzll((long long)d.mant) + ee);
       }
       float w[EPT][7];
       uint32_t lb[EPT];
@@ -365,35 +388,34 @@ __global__ void k_accu_exponents(const int32_t *__restrict__ bound, const int32_
 
 }  // namespace
 
-cudaError_t launch_row_scale(int mode, const double *XA, long lda, int rowsA, int32_t *eA,
-                             int32_t *EA, void *barsA, const double *XB, long ldb, int rowsB,
-                             int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
+cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int rowsA,
+                             int32_t *eA, int32_t *EA, void *barsA, const void *XB, long ldb,
+                             int rowsB, int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
                              const Os2Tables *t, int *status, cudaStream_t s) {
   if (rowsA + rowsB <= 0) return cudaSuccess;
   RowSet a{XA, lda, rowsA, eA, EA, reinterpret_cast<__half *>(barsA)};
   RowSet b{XB, ldb, rowsB, eB, EB, reinterpret_cast<__half *>(barsB)};
   dim3 grid(rowsA + rowsB);
-  if (mode == SM_BARS)
-    k_row_scale<SM_BARS><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
-  else
-    k_row_scale<SM_FAST_SCALE><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+  if (mode == SM_BARS) {
+    if (f32) k_row_scale<SM_BARS, float><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    else k_row_scale<SM_BARS, double><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+  } else {
+    if (f32) k_row_scale<SM_FAST_SCALE, float><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    else k_row_scale<SM_FAST_SCALE, double><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+  }
   return cudaGetLastError();
 }
 
-cudaError_t launch_residues(const double *XA, long lda, int rowsA, const int32_t *eA,
-                            void *planesA, const double *XB, long ldb, int rowsB,
-                            const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
-                            cudaStream_t s) {
-  if (rowsA + rowsB <= 0 || kp <= 0) return cudaSuccess;
-  RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA)};
-  RowSet b{XB, ldb, rowsB, const_cast<int32_t *>(eB), nullptr, reinterpret_cast<__half *>(planesB)};
+template <typename T>
+cudaError_t residues_t(const RowSet &a, const RowSet &b, int k, int kp, const Os2Tables *t,
+                       cudaStream_t s) {
   const int cpr = kp / kEPT;
   const int bx = (cpr + kThreads - 1) / kThreads;
-  const int rows = rowsA + rowsB;
+  const int rows = a.rows + b.rows;
   dim3 grid(bx, rows < 65535 ? rows : 65535);
 #define OS2_CASE(NN)                                                         \
   case NN:                                                                   \
-    k_residues<NN><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res);           \
+    k_residues<NN, T><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res);        \
     break;
   switch (t->N) {
     OS2_CASE(1) OS2_CASE(2) OS2_CASE(3) OS2_CASE(4) OS2_CASE(5) OS2_CASE(6) OS2_CASE(7)
@@ -403,6 +425,16 @@ cudaError_t launch_residues(const double *XA, long lda, int rowsA, const int32_t
   }
 #undef OS2_CASE
   return cudaGetLastError();
+}
+
+cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const int32_t *eA,
+                            void *planesA, const void *XB, long ldb, int rowsB,
+                            const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
+                            cudaStream_t s) {
+  if (rowsA + rowsB <= 0 || kp <= 0) return cudaSuccess;
+  RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA)};
+  RowSet b{XB, ldb, rowsB, const_cast<int32_t *>(eB), nullptr, reinterpret_cast<__half *>(planesB)};
+  return f32 ? residues_t<float>(a, b, k, kp, t, s) : residues_t<double>(a, b, k, kp, t, s);
 }
 
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,

@@ -266,8 +266,8 @@ T *at(void *ws, size_t off) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-os2_status check_gemm_args(int m, int n, int k, const double *A, int lda, const double *B,
-                           int ldb, const double *C, int ldc, int N, int mode) {
+os2_status check_gemm_args(int m, int n, int k, const void *A, int lda, const void *B, int ldb,
+                           const void *C, int ldc, int N, int mode, size_t esize = 8) {
   if (m < 0 || n < 0 || k < 0) return OS2_ERR_INVALID_ARG;
   if (N < 1 || N > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
   if (mode != OS2_MODE_FAST && mode != OS2_MODE_ACCURATE) return OS2_ERR_INVALID_ARG;
@@ -277,17 +277,18 @@ os2_status check_gemm_args(int m, int n, int k, const double *A, int lda, const 
   if (m > 0 && n > 0 && !C) return OS2_ERR_INVALID_ARG;
   if (m > 0 && k > 0 && !A) return OS2_ERR_INVALID_ARG;
   if (n > 0 && k > 0 && !B) return OS2_ERR_INVALID_ARG;
-  if ((A && !aligned(A, 8)) || (B && !aligned(B, 8)) || (C && !aligned(C, 8)))
+  if ((A && !aligned(A, esize)) || (B && !aligned(B, esize)) || (C && !aligned(C, esize)))
     return OS2_ERR_INVALID_ARG;
   return OS2_OK;
 }
 
-// The five steps on device operands; arguments already checked.
-os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
-                    double *C, int ldc, int N, int mode, void *ws, const Layout &L,
-                    cudaStream_t s) {
+// The five steps on device operands; arguments already checked.  f32: float
+// operands and result (SGEMM emulation), else double.
+os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const void *B, int ldb,
+                    void *C, int ldc, int N, int mode, void *ws, const Layout &L, cudaStream_t s) {
+  const size_t es = f32 ? 4 : 8;
   if (m == 0 || n == 0) return OS2_OK;
-  if (k == 0) return cuda_status(cudaMemset2DAsync(C, (size_t)ldc * 8, 0, (size_t)n * 8, m, s));
+  if (k == 0) return cuda_status(cudaMemset2DAsync(C, (size_t)ldc * es, 0, (size_t)n * es, m, s));
   const Os2Tables *t = os2_tables(N);
   int *status = os2_status_ptr();
   if (!t || !status) return OS2_ERR_CUDA;
@@ -298,7 +299,7 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
   if (mode == OS2_MODE_FAST) {
     // step 1: exponents from the revised bound (A's rows and B's columns)
     ProfScope ps("scale", s);
-    if ((err = launch_row_scale(SM_FAST_SCALE, A, lda, m, e, nullptr, nullptr, B, ldb, n, f,
+    if ((err = launch_row_scale(SM_FAST_SCALE, f32, A, lda, m, e, nullptr, nullptr, B, ldb, n, f,
                                 nullptr, nullptr, k, L.kp, t, status, s)))
       return cuda_status(err);
   } else {
@@ -308,8 +309,8 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
     int32_t *R = at<int32_t>(ws, L.R), *K = at<int32_t>(ws, L.K);
     {
       ProfScope ps("scale_bars", s);
-      if ((err = launch_row_scale(SM_BARS, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB, pb,
-                                  k, L.kp, t, status, s)))
+      if ((err = launch_row_scale(SM_BARS, f32, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB,
+                                  pb, k, L.kp, t, status, s)))
         return cuda_status(err);
     }
     if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
@@ -325,7 +326,7 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
   // step 2: residue planes of A and B
   {
     ProfScope ps("residues", s);
-    if ((err = launch_residues(A, lda, m, e, pa, B, ldb, n, f, pb, k, L.kp, t, s)))
+    if ((err = launch_residues(f32, A, lda, m, e, pa, B, ldb, n, f, pb, k, L.kp, t, s)))
       return cuda_status(err);
   }
   // step 3
@@ -341,7 +342,7 @@ os2_status run_gemm(int m, int n, int k, const double *A, int lda, const double 
   }
   // steps 4 + 5
   ProfScope ps("crt_unscale", s);
-  return cuda_status(launch_crt(m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
+  return cuda_status(launch_crt(f32, m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
 }
 
 }  // namespace
@@ -367,7 +368,22 @@ os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double 
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
       return OS2_ERR_WORKSPACE;
   }
-  return run_gemm(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
+  return run_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
+                  static_cast<cudaStream_t>(stream));
+}
+
+os2_status os2_sgemm(int m, int n, int k, const float *A, int lda, const float *B, int ldb,
+                     float *C, int ldc, int num_moduli, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  os2_status st = check_gemm_args(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, 4);
+  if (st) return st;
+  Layout L;
+  make_layout(m, n, k, num_moduli, mode, &L);
+  if (m > 0 && n > 0 && k > 0) {
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
+      return OS2_ERR_WORKSPACE;
+  }
+  return run_gemm(true, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
                   static_cast<cudaStream_t>(stream));
 }
 
@@ -403,7 +419,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
                                  cudaMemcpyHostToDevice, s)))
       return cuda_status(err);
   }
-  st = run_gemm(m, n, k, dA, kk, dB, kk, dC, n, num_moduli, mode, workspace, L, s);
+  st = run_gemm(false, m, n, k, dA, kk, dB, kk, dC, n, num_moduli, mode, workspace, L, s);
   if (st) return st;
   return cuda_status(cudaMemcpy2DAsync(C, 8 * (size_t)ldc, dC, 8 * (size_t)n, 8 * (size_t)n, m,
                                        cudaMemcpyDeviceToHost, s));
@@ -430,16 +446,16 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
     return OS2_OK;
   }
   if (mode == OS2_MODE_FAST)
-    return cuda_status(launch_row_scale(SM_FAST_SCALE, A, lda, m, e, nullptr, nullptr, B, ldb, n,
-                                        f, nullptr, nullptr, k, 0, t, status, s));
+    return cuda_status(launch_row_scale(SM_FAST_SCALE, false, A, lda, m, e, nullptr, nullptr, B,
+                                        ldb, n, f, nullptr, nullptr, k, 0, t, status, s));
   Layout L;
   make_layout(m, n, k, 1, mode, &L);
   if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return OS2_ERR_WORKSPACE;
   int32_t *EA = at<int32_t>(workspace, L.EA), *EB = at<int32_t>(workspace, L.EB);
   int32_t *R = at<int32_t>(workspace, L.R), *K = at<int32_t>(workspace, L.K);
   void *pa = at<void>(workspace, L.planesA), *pb = at<void>(workspace, L.planesB);
-  if ((err = launch_row_scale(SM_BARS, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB, pb, k,
-                              L.kp, t, status, s)))
+  if ((err = launch_row_scale(SM_BARS, false, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB,
+                              pb, k, L.kp, t, status, s)))
     return cuda_status(err);
   if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)std::max(m, 1), s))) return cuda_status(err);
   if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)std::max(n, 1), s))) return cuda_status(err);
@@ -461,8 +477,8 @@ os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t
   const Os2Tables *t = os2_tables(num_moduli);
   int *status = os2_status_ptr();
   if (!t || !status) return OS2_ERR_CUDA;
-  return cuda_status(launch_residues(X, ldx, rows, exps, planes, nullptr, 0, 0, nullptr, nullptr, k,
-                                     ldp, t, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_residues(false, X, ldx, rows, exps, planes, nullptr, 0, 0, nullptr,
+                                     nullptr, k, ldp, t, static_cast<cudaStream_t>(stream)));
 }
 
 os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB, int ldp,
@@ -505,7 +521,7 @@ os2_status os2_crt(int m, int n, const int8_t *c, int ldcres, int num_moduli, co
   if (!c || !e || !f || !C || !aligned(c, 4) || !aligned(C, 8)) return OS2_ERR_INVALID_ARG;
   const Os2Tables *t = os2_tables(num_moduli);
   if (!t) return OS2_ERR_CUDA;
-  return cuda_status(launch_crt(m, n, c, ldcres, e, f, C, ldc, X_out, t,
+  return cuda_status(launch_crt(false, m, n, c, ldcres, e, f, C, ldc, X_out, t,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -642,6 +658,6 @@ extern "C" os2_status os2_gemm_noalloc(int m, int n, int k, const double *A, int
   if (L.total > (size_t)OS2_NOALLOC_SCRATCH_BYTES) return OS2_ERR_WORKSPACE;
   void *ws = noalloc_scratch();
   if (!ws) return OS2_ERR_CUDA;
-  return run_gemm(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, ws, L,
+  return run_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, ws, L,
                   static_cast<cudaStream_t>(stream));
 }

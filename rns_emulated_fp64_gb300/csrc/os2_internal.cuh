@@ -67,18 +67,20 @@ enum ScaleMode {
 
 // Launchers (return cudaError_t of the launch).  Each handles A's rows and
 // B's columns (rows of Bt) in one launch; pass rowsB = 0 for one operand.
-cudaError_t launch_row_scale(int mode, const double *XA, long lda, int rowsA, int32_t *eA,
-                             int32_t *EA, void *barsA, const double *XB, long ldb, int rowsB,
-                             int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
+// f32: the operands are float (SGEMM emulation) instead of double.
+cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int rowsA,
+                             int32_t *eA, int32_t *EA, void *barsA, const void *XB, long ldb,
+                             int rowsB, int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
                              const Os2Tables *t, int *status, cudaStream_t s);
-cudaError_t launch_residues(const double *XA, long lda, int rowsA, const int32_t *eA,
-                            void *planesA, const double *XB, long ldb, int rowsB,
+cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const int32_t *eA,
+                            void *planesA, const void *XB, long ldb, int rowsB,
                             const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
                             cudaStream_t s);
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,
                                   const Os2Tables *t, cudaStream_t s);
-cudaError_t launch_crt(int m, int n, const int8_t *c, int ldcres, const int32_t *e,
-                       const int32_t *f, double *C, int ldc, uint32_t *X_out, const Os2Tables *t,
+// f32: C is float (correctly rounded to binary32) instead of double.
+cudaError_t launch_crt(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
+                       const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
                        cudaStream_t s);
 cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *RB, int N,
                              int out_kind, void *out, int ldo, const Os2Tables *t, cudaStream_t s);

@@ -383,3 +383,58 @@ def test_modp_products_far_beyond_int32():
             r = (16384 * k) % p
             r = r - p if r >= (p + 1) // 2 else r
             assert np.all(c[l] == r), (variant, p)
+
+
+# ------------------------------------------------------------ SGEMM emulation --
+def _f32_bits_equal(got, want, what):
+    got = np.ascontiguousarray(got, np.float32)
+    want = np.ascontiguousarray(want, np.float32)
+    bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+    assert bad.size == 0, f"{what}: {bad.size} entries differ, first {bad[:5]}"
+
+
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+@pytest.mark.parametrize("N,m,n,k", [(7, 64, 64, 64), (4, 129, 257, 65), (8, 300, 200, 1000),
+                                     (10, 130, 140, 1921), (14, 33, 65, 3000)])
+def test_sgemm_parity(mode, N, m, n, k):
+    """SGEMM emulation ([G] Ergebnisse): float operands, binary32 result,
+    bit-exact against the oracle rounding the same CRT integer to binary32."""
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=N + k, phi=1.0)
+    A = A.astype(np.float32)
+    Bt = Bt.astype(np.float32)
+    C = os2.sgemm(dev(A), dev(Bt), N, mode).cpu().numpy()
+    status_ok()
+    ref = orc.gemm_entries(A, Bt, N, mode=orc.FAST if mode == "fast" else orc.ACCURATE,
+                           want_X=False, want_c=False, want_G=False, out_f32=True)
+    assert ref.mismatches == 0
+    _f32_bits_equal(C, ref.C, f"sgemm {mode} N={N} {m}x{n}x{k}")
+
+
+def test_sgemm_edge_values():
+    rng = np.random.default_rng(4)
+    A = rng.standard_normal((40, 96)).astype(np.float32)
+    Bt = rng.standard_normal((50, 96)).astype(np.float32)
+    A[0] = 0
+    A[1, ::2] = np.float32(1e-45)          # float subnormals
+    A[2] *= np.float32(1e37)
+    Bt[3] *= np.float32(1e-30)
+    Bt[4, 5] = np.float32(3e38)
+    for mode, om in (("fast", orc.FAST), ("accurate", orc.ACCURATE)):
+        C = os2.sgemm(dev(A), dev(Bt), 8, mode).cpu().numpy()
+        status_ok()
+        ref = orc.gemm_entries(A, Bt, 8, mode=om, want_X=False, want_c=False, want_G=False,
+                               out_f32=True)
+        _f32_bits_equal(C, ref.C, f"sgemm edges {mode}")
+
+
+def test_sgemm_4096cube_sample():
+    A, Bt = workloads.make_pair("spread", 4096, 4096, 4096, seed=0, phi=0.5)
+    A = A.astype(np.float32)
+    Bt = Bt.astype(np.float32)
+    C = os2.sgemm(dev(A), dev(Bt), 7, "fast")
+    status_ok()
+    rows, cols = workloads.sample_grid(4096, 4096, 32, seed=1)
+    ref = orc.gemm_entries(A, Bt, 7, rows, cols, want_X=False, want_c=False, want_G=False,
+                           out_f32=True)
+    got = C.cpu().numpy()[np.ix_(rows, cols)]
+    _f32_bits_equal(got, ref.C, "sgemm 4096^3 sample")

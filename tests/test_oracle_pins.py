@@ -365,3 +365,55 @@ def test_nonfinite_rejected():
     A[1, 2] = np.inf
     with pytest.raises(orc.OracleError):
         orc.scale_fast(A, 14)
+
+
+# ------------------------------------------------------- SGEMM emulation ----
+def _round_fraction(fr, prec, emin, emax):
+    """Correct RN-even rounding of a rational to a binary format (reference)."""
+    if fr == 0:
+        return 0.0
+    sign = -1.0 if fr < 0 else 1.0
+    a = abs(fr)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = max(e, emin) - (prec - 1)
+    scaled = a / Fraction(2) ** q
+    n = scaled.numerator // scaled.denominator
+    rem = scaled - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = Fraction(n) * Fraction(2) ** q
+    if val >= Fraction(2) ** (emax + 1):
+        return sign * math.inf
+    return sign * float(val)
+
+
+def test_round_scaled_f32_against_fraction():
+    """Binary32 unscale (SGEMM emulation, [G] Ergebnisse): one RN-even rounding
+    to 24 bits, subnormals down to 2^-149, overflow at 2^128."""
+    rnd = random.Random(11)
+    cases = [(1, 149), (1, 150), (3, 151), (2 ** 24 + 1, 0), (-(2 ** 25 + 3), 1), (1, -127), (3, -127),
+             ((1 << 24) - 1, -104), ((1 << 25) - 1, -104)]
+    for _ in range(3000):
+        X = rnd.getrandbits(rnd.randint(1, 160)) * rnd.choice((1, -1))
+        cases.append((X, rnd.randint(-300, 400)))
+        base = rnd.getrandbits(24) | (1 << 23)
+        sh = rnd.randint(1, 60)
+        cases.append(((2 * base + 1) << (sh - 1), sh + rnd.randint(-150, 150)))
+    for X, s in cases:
+        want = _round_fraction(Fraction(X) / Fraction(2) ** s, 24, -126, 127) if X else 0.0
+        got = orc.round_scaled_f32(X, s)
+        assert got == want or (math.isinf(got) and math.isinf(want)), (X, s, got, want)
+        assert math.copysign(1, got) == math.copysign(1, want), (X, s)
+        if not math.isinf(got):
+            assert float(np.float32(got)) == got      # representable in binary32
+
+
+def test_sgemm_oracle_integer_inputs_exact():
+    A, Bt = workloads.make_pair("int", 12, 10, 50, seed=1, phi=100)
+    r = orc.gemm_entries(A.astype(np.float32), Bt.astype(np.float32), 7, out_f32=True)
+    assert r.C.dtype == np.float32
+    assert np.array_equal(r.C, (A @ Bt.T).astype(np.float32))
