@@ -434,6 +434,25 @@ def run_ours(a):
         line["sgemm_8192cube_N7_fast"] = {"ms": sms, "tflops": flop / (sms / 1e3) / 1e12}
         del Af, Bf, Cf, wsf
         torch.cuda.empty_cache()
+        # ZGEMM emulation at 4096^3 complex (8mnk real flop), 16 moduli, fast mode
+        mz = 4096
+        Zr, Zi = workloads.make_pair("spread", mz, mz, mz, seed=rank, phi=a.phi)
+        Za = torch.complex(torch.from_numpy(Zr[:, :mz]), torch.from_numpy(Zi[:, :mz])).to(dev)
+        Zb = torch.complex(torch.from_numpy(Zi[:, :mz].copy()), torch.from_numpy(Zr[:, :mz].copy())).to(dev)
+        wsz = os2.alloc_workspace(os2.complex_workspace_size(mz, mz, mz, 16, "fast"), dev)
+        Cz = torch.empty((mz, mz), dtype=torch.complex128, device=dev)
+        for _ in range(2):
+            os2.zgemm(Za, Zb, 16, "fast", out=Cz, workspace=wsz, stream=stream)
+        torch.cuda.synchronize(dev)
+        s0.record(stream)
+        for _ in range(5):
+            os2.zgemm(Za, Zb, 16, "fast", out=Cz, workspace=wsz, stream=stream)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        zms = s0.elapsed_time(s1) / 5
+        line["zgemm_4096cube_N16_fast"] = {"ms": zms, "tflops": 8.0 * mz ** 3 / (zms / 1e3) / 1e12}
+        del Za, Zb, wsz, Cz
+        torch.cuda.empty_cache()
 
     # context: native cuBLAS DGEMM rate and accuracy against the exact product
     if rank == 0 and not a.no_context:

@@ -105,6 +105,24 @@ os2_status os2_sgemm(int m, int n, int k, const float *A, int lda, const float *
                      float *C, int ldc, int num_moduli, int mode, void *workspace,
                      size_t workspace_bytes, void *stream);
 
+/* Complex products ([G] "Bedeutung": the approach extends to ZGEMM/CGEMM).
+ * A complex product is computed as the real block product
+ *   [C_r | C_i] = [A_r | A_i] . [[B_r, B_i], [-B_i, B_r]]   (m x 2n x 2k),
+ * so the scaling uses complex row/column norms (|a_r|^2 + |a_i|^2), every
+ * integer product is exact and the CRT bound covers both parts.
+ * Layouts: complex entries interleaved (re, im).  A is m x k row-major with
+ * lda >= k complex entries per row; B is k x n column-major with ldb >= k
+ * complex entries per column; C is m x n row-major with ldc >= n.  Workspace:
+ * os2_complex_workspace_size(m, n, k, N, mode, single) bytes (single = 1 for
+ * CGEMM), 256-byte aligned.  Other conventions as os2_gemm / os2_sgemm. */
+size_t os2_complex_workspace_size(int m, int n, int k, int num_moduli, int mode, int single);
+os2_status os2_zgemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                     double *C, int ldc, int num_moduli, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream);
+os2_status os2_cgemm(int m, int n, int k, const float *A, int lda, const float *B, int ldb,
+                     float *C, int ldc, int num_moduli, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
 /* Device workspace for os2_gemm_host: os2_workspace_size plus device copies
  * of A (m*k), B (k*n) and C (m*n) doubles. */
 size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode);

@@ -272,3 +272,41 @@ def gemm_entries(A, Bt, N: int, rows=None, cols=None, mode: int = FAST, e=None, 
 
 def X_int(ent: Entries, a: int, b: int) -> int:
     return limbs_to_int(ent.X[a, b])
+
+
+# --------------------------------------------------------------------------
+# complex products
+# --------------------------------------------------------------------------
+def stack_complex(A, Bt):
+    """The real block form of a complex product: C_r = [A_r|A_i].[B_r;-B_i],
+    C_i = [A_r|A_i].[B_i;B_r].  Returns (A2 m x 2k, Bt2 2n x 2k) as float64
+    (complex64 parts are exact in float64)."""
+    A = np.asarray(A)
+    Bt = np.asarray(Bt)
+    A2 = np.ascontiguousarray(np.concatenate([A.real, A.imag], axis=1), dtype=np.float64)
+    Br = np.concatenate([Bt.real, -Bt.imag], axis=1)
+    Bi = np.concatenate([Bt.imag, Bt.real], axis=1)
+    Bt2 = np.ascontiguousarray(np.concatenate([Br, Bi], axis=0), dtype=np.float64)
+    return A2, Bt2
+
+
+def complex_gemm_entries(A, Bt, N: int, rows=None, cols=None, mode: int = FAST,
+                         single: bool = False):
+    """Oracle of the emulated complex product for the entries rows x cols:
+    the real oracle on the block form (rows of A2, columns j and n + j)."""
+    A2, Bt2 = stack_complex(A, Bt)
+    n = np.asarray(Bt).shape[0]
+    m = np.asarray(A).shape[0]
+    rows = np.arange(m, dtype=np.int32) if rows is None else np.asarray(rows, np.int32)
+    cols = np.arange(n, dtype=np.int32) if cols is None else np.asarray(cols, np.int32)
+    cols2 = np.concatenate([cols, cols + n]).astype(np.int32)
+    if mode == ACCURATE:
+        e, f = scale_accu(A2, Bt2, N, rows, cols2)
+        r = gemm_entries(A2, Bt2, N, rows, cols2, mode=ACCURATE, e=e, f=f, want_X=False,
+                         want_c=False, want_G=False, out_f32=single)
+    else:
+        r = gemm_entries(A2, Bt2, N, rows, cols2, want_X=False, want_c=False, want_G=False,
+                         out_f32=single)
+    nc = len(cols)
+    C = r.C[:, :nc] + 1j * r.C[:, nc:]
+    return C.astype(np.complex64 if single else np.complex128), r

@@ -7,5 +7,5 @@ from .binding import (GEMM_SIMT, GEMM_TC, GEMM_TC_1SM, MODE_ACCURATE, MODE_FAST,
                       OUT_RAW_INT32, Os2Error, alloc_workspace, crt, gemm, gemm_host,
                       gemm_residues, get_status, host_workspace_size, launch_count, load,
                       matmul, moduli, profile_start, profile_stop, residues, scale, sgemm,
-                      set_gemm_variant, status_string,
-                      workspace_size)
+                      set_gemm_variant, status_string, workspace_size, zgemm,
+                      complex_workspace_size)

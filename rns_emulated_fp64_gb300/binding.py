@@ -26,7 +26,8 @@ EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gem
            "os2_scale", "os2_residues", "os2_gemm_residues", "os2_crt", "os2_moduli",
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
            "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
-           "os2_gemm_noalloc", "os2_sgemm")
+           "os2_gemm_noalloc", "os2_sgemm", "os2_complex_workspace_size", "os2_zgemm",
+           "os2_cgemm")
 
 _lib = None
 _lock = threading.Lock()
@@ -89,6 +90,12 @@ def load(build_if_missing: bool = True):
         L.os2_gemm_noalloc.restype = i
         L.os2_sgemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
         L.os2_sgemm.restype = i
+        L.os2_complex_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.os2_complex_workspace_size.restype = sz
+        L.os2_zgemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
+        L.os2_zgemm.restype = i
+        L.os2_cgemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
+        L.os2_cgemm.restype = i
         _lib = L
         return L
 
@@ -202,6 +209,39 @@ def sgemm(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 7, mode="fast", o
                           num_moduli, _mode(mode), _ptr(workspace), workspace.numel(),
                           _stream(stream))
     _check(st, "os2_sgemm")
+    return out
+
+
+def complex_workspace_size(m, n, k, num_moduli, mode="fast", single=False) -> int:
+    return int(load().os2_complex_workspace_size(m, n, k, num_moduli, _mode(mode), int(single)))
+
+
+def zgemm(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 16, mode="fast", out=None,
+          workspace=None, stream=None) -> torch.Tensor:
+    """C = A @ Bt.T for complex operands (complex128 -> ZGEMM, complex64 -> CGEMM).
+
+    A: m x k, Bt: n x k (B = Bt.T column-major), complex CUDA tensors with
+    contiguous rows (interleaved re/im).  Returns C (m x n) of the same dtype."""
+    if A.dtype not in (torch.complex128, torch.complex64) or Bt.dtype != A.dtype:
+        raise ValueError("A and Bt must both be complex128 or both complex64")
+    for X, nm in ((A, "A"), (Bt, "Bt")):
+        if not (X.is_cuda and X.dim() == 2 and X.stride(1) == 1):
+            raise ValueError(f"{nm} must be a 2-D CUDA tensor with contiguous rows")
+    single = A.dtype == torch.complex64
+    m, k = A.shape
+    n = Bt.shape[0]
+    if Bt.shape[1] != k:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((m, n), dtype=A.dtype, device=A.device)
+    if workspace is None:
+        workspace = alloc_workspace(complex_workspace_size(m, n, k, num_moduli, mode, single),
+                                    A.device)
+    fn = load().os2_cgemm if single else load().os2_zgemm
+    st = fn(m, n, k, _ptr(A), max(A.stride(0), max(k, 1)), _ptr(Bt), max(Bt.stride(0), max(k, 1)),
+            _ptr(out), max(out.stride(0), max(n, 1)), num_moduli, _mode(mode), _ptr(workspace),
+            workspace.numel(), _stream(stream))
+    _check(st, "os2_cgemm" if single else "os2_zgemm")
     return out
 
 

@@ -387,6 +387,68 @@ os2_status os2_sgemm(int m, int n, int k, const float *A, int lda, const float *
                   static_cast<cudaStream_t>(stream));
 }
 
+// Complex products: the real workspace of the stacked m x 2n x 2k product,
+// then A2 (m x 2k), Bt2 (2n x 2k) and C2 (m x 2n) in the element type.
+static bool complex_layout(int m, int n, int k, int N, int mode, size_t es, Layout *L,
+                           size_t *offA2, size_t *offB2, size_t *offC2, size_t *total) {
+  if (m < 0 || n < 0 || k < 0 || n > (1 << 30) || k > (1 << 30)) return false;
+  if (!make_layout(m, 2 * n, 2 * k, N, mode, L)) return false;
+  *offA2 = L->total;
+  *offB2 = *offA2 + os2_round_up(es * (size_t)m * 2 * k, 256);
+  *offC2 = *offB2 + os2_round_up(es * (size_t)2 * n * 2 * k, 256);
+  *total = *offC2 + os2_round_up(es * (size_t)m * 2 * n, 256);
+  return true;
+}
+
+static os2_status complex_gemm(bool f32, int m, int n, int k, const void *A, int lda,
+                               const void *B, int ldb, void *C, int ldc, int N, int mode,
+                               void *ws, size_t wsb, cudaStream_t s) {
+  const size_t es = f32 ? 4 : 8;
+  if (m < 0 || n < 0 || k < 0 || lda < std::max(k, 1) || ldb < std::max(k, 1) ||
+      ldc < std::max(n, 1))
+    return OS2_ERR_INVALID_ARG;
+  // the stacked product has inner dimension 2k
+  os2_status st = check_gemm_args(m, 2 * n, 2 * k, A, 2 * lda, B, 2 * ldb, C, 2 * ldc, N, mode, es);
+  if (st) return st;
+  Layout L;
+  size_t oA, oB, oC, total;
+  if (!complex_layout(m, n, k, N, mode, es, &L, &oA, &oB, &oC, &total)) return OS2_ERR_INVALID_ARG;
+  if (m == 0 || n == 0) return OS2_OK;
+  if (!ws || wsb < total || !aligned(ws, 256)) return OS2_ERR_WORKSPACE;
+  void *A2 = at<char>(ws, oA), *B2 = at<char>(ws, oB), *C2 = at<char>(ws, oC);
+  cudaError_t err;
+  {
+    ProfScope ps("complex_stack", s);
+    if ((err = launch_complex_stack(f32, m, n, k, A, lda, B, ldb, A2, B2, s))) return cuda_status(err);
+  }
+  st = run_gemm(f32, m, 2 * n, 2 * k, A2, std::max(2 * k, 1), B2, std::max(2 * k, 1), C2,
+                2 * n, N, mode, ws, L, s);
+  if (st) return st;
+  ProfScope ps("complex_unstack", s);
+  return cuda_status(launch_complex_unstack(f32, m, n, C2, C, ldc, s));
+}
+
+size_t os2_complex_workspace_size(int m, int n, int k, int num_moduli, int mode, int single) {
+  Layout L;
+  size_t a, b, c, total;
+  return complex_layout(m, n, k, num_moduli, mode, single ? 4 : 8, &L, &a, &b, &c, &total) ? total
+                                                                                          : 0;
+}
+
+os2_status os2_zgemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
+                     double *C, int ldc, int num_moduli, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  return complex_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+os2_status os2_cgemm(int m, int n, int k, const float *A, int lda, const float *B, int ldb,
+                     float *C, int ldc, int num_moduli, int mode, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+  return complex_gemm(true, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode) {
   Layout L;
   if (!make_layout(m, n, k, num_moduli, mode, &L)) return 0;

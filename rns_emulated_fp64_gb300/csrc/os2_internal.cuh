@@ -92,4 +92,10 @@ cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const
                            int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,
                            int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s);
 
+// Complex products: interleaved complex operands <-> stacked real operands.
+cudaError_t launch_complex_stack(bool f32, int m, int n, int k, const void *A, long lda,
+                                 const void *B, long ldb, void *A2, void *Bt2, cudaStream_t s);
+cudaError_t launch_complex_unstack(bool f32, int m, int n, const void *C2, void *C, long ldc,
+                                   cudaStream_t s);
+
 static inline size_t os2_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -438,3 +438,33 @@ def test_sgemm_4096cube_sample():
                            out_f32=True)
     got = C.cpu().numpy()[np.ix_(rows, cols)]
     _f32_bits_equal(got, ref.C, "sgemm 4096^3 sample")
+
+
+# ------------------------------------------------------------- ZGEMM / CGEMM --
+@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+@pytest.mark.parametrize("m,n,k", [(1, 1, 1), (64, 64, 64), (129, 65, 100), (200, 150, 700)])
+def test_complex_parity(single, mode, m, n, k):
+    """[G] Bedeutung: ZGEMM/CGEMM through the real block form, bit-exact
+    against the oracle of the same block form."""
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=k, phi=1.0)        # real parts
+    Ai, Bi = workloads.make_pair("spread", m, n, k, seed=k + 1, phi=1.0)  # imaginary parts
+    Z = (A + 1j * Ai).astype(np.complex64 if single else np.complex128)
+    W = (Bt + 1j * Bi).astype(np.complex64 if single else np.complex128)
+    N = 8 if single else 16
+    C = os2.zgemm(dev(Z), dev(W), N, mode).cpu().numpy()
+    status_ok()
+    ref, r = orc.complex_gemm_entries(Z, W, N, mode=orc.FAST if mode == "fast" else orc.ACCURATE,
+                                      single=single)
+    assert r.mismatches == 0
+    assert np.array_equal(C.view(np.uint32 if single else np.uint64),
+                          ref.view(np.uint32 if single else np.uint64))
+
+
+def test_zgemm_integer_inputs_exact_on_gpu():
+    rng = np.random.default_rng(9)
+    Z = rng.integers(-99, 100, (70, 90)) + 1j * rng.integers(-99, 100, (70, 90))
+    W = rng.integers(-99, 100, (50, 90)) + 1j * rng.integers(-99, 100, (50, 90))
+    C = os2.zgemm(dev(Z.astype(np.complex128)), dev(W.astype(np.complex128)), 14).cpu().numpy()
+    status_ok()
+    assert np.array_equal(C, Z @ W.T)

@@ -417,3 +417,44 @@ def test_sgemm_oracle_integer_inputs_exact():
     r = orc.gemm_entries(A.astype(np.float32), Bt.astype(np.float32), 7, out_f32=True)
     assert r.C.dtype == np.float32
     assert np.array_equal(r.C, (A @ Bt.T).astype(np.float32))
+
+
+# ------------------------------------------------------------ complex --------
+def test_complex_oracle_integer_inputs_exact():
+    """[G] Bedeutung (ZGEMM/CGEMM): the block form reproduces the complex
+    product; small-integer complex inputs give it exactly."""
+    rng = np.random.default_rng(3)
+    A = rng.integers(-50, 51, (9, 23)) + 1j * rng.integers(-50, 51, (9, 23))
+    Bt = rng.integers(-50, 51, (7, 23)) + 1j * rng.integers(-50, 51, (7, 23))
+    C, r = orc.complex_gemm_entries(A, Bt, 14)
+    assert r.mismatches == 0
+    assert np.array_equal(C, A @ Bt.T)
+    Cs, _ = orc.complex_gemm_entries(A.astype(np.complex64), Bt.astype(np.complex64), 8, single=True)
+    assert np.array_equal(Cs, (A @ Bt.T).astype(np.complex64))
+
+
+def test_complex_scaling_uses_complex_norms():
+    """The stacked row norm is the complex row norm: mu_i^2 sum_h |a_ih|^2 <= H."""
+    rng = np.random.default_rng(5)
+    A = rng.standard_normal((6, 30)) + 1j * rng.standard_normal((6, 30)) * 4.0
+    A2, _ = orc.stack_complex(A, np.zeros((1, 30), complex))
+    for N in (8, 16):
+        _, H, _, _ = orc.tables(N)
+        e = orc.scale_fast(A2, N)
+        for i in range(6):
+            norm2 = sum(Fraction(float(z.real)) ** 2 + Fraction(float(z.imag)) ** 2 for z in A[i])
+            assert Fraction(4) ** int(e[i]) * norm2 <= H
+
+
+def test_complex_emulation_error_small():
+    A, Bt = workloads.make_pair("normal", 5, 4, 40, seed=2)
+    Ai, Bi = workloads.make_pair("normal", 5, 4, 40, seed=3)
+    Z, W = A + 1j * Ai, Bt + 1j * Bi
+    C, _ = orc.complex_gemm_entries(Z, W, 16)
+    for i in range(5):
+        for j in range(4):
+            re = sum(Fraction(float(a.real)) * Fraction(float(b.real)) - Fraction(float(a.imag)) * Fraction(float(b.imag)) for a, b in zip(Z[i], W[j]))
+            im = sum(Fraction(float(a.real)) * Fraction(float(b.imag)) + Fraction(float(a.imag)) * Fraction(float(b.real)) for a, b in zip(Z[i], W[j]))
+            scale = float(sum(abs(a) * abs(b) for a, b in zip(Z[i], W[j])))
+            assert abs(float(Fraction(C[i, j].real) - re)) <= 2.0 ** -48 * scale
+            assert abs(float(Fraction(C[i, j].imag) - im)) <= 2.0 ** -48 * scale
