@@ -324,15 +324,22 @@ def test_scale_invariance_on_gpu(s):
         assert_bits_equal(Css, np.ldexp(C0, 2 * s), f"A,B*2^{s}")
 
 
-def test_host_entry_point_matches_device():
-    A, Bt = workloads.make_pair("spread", 100, 120, 300, seed=6, phi=2.0)
-    Ah = torch.from_numpy(A).pin_memory()
-    Bh = torch.from_numpy(Bt).pin_memory()
-    Ch = torch.empty((100, 120), dtype=torch.float64).pin_memory()
-    os2.gemm_host(Ah, Bh, Ch, 14)
-    torch.cuda.synchronize()
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+@pytest.mark.parametrize("m,n,k,pinned", [(100, 120, 300, True), (1001, 700, 513, True),
+                                          (3, 2, 5, False)])
+def test_host_entry_point_matches_device(mode, m, n, k, pinned):
+    """The end-to-end host entry point (copies in, five steps, copy out; fast
+    mode pipelines the copies with the kernels) equals the device one."""
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=6, phi=2.0)
+    Ah = torch.from_numpy(A)
+    Bh = torch.from_numpy(Bt)
+    Ch = torch.full((m, n), np.nan, dtype=torch.float64)
+    if pinned:
+        Ah, Bh, Ch = Ah.pin_memory(), Bh.pin_memory(), Ch.pin_memory()
+    os2.gemm_host(Ah, Bh, Ch, 14, mode)
+    torch.cuda.current_stream().synchronize()
     status_ok()
-    Cd = os2.gemm(dev(A), dev(Bt), 14).cpu().numpy()
+    Cd = os2.gemm(dev(A), dev(Bt), 14, mode).cpu().numpy()
     assert_bits_equal(Ch.numpy(), Cd, "host vs device entry")
 
 
