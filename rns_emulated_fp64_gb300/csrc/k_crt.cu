@@ -160,74 +160,6 @@ __device__ __forceinline__ OutT round_scaled_fast(const uint32_t (&m)[L], bool n
   return ex > F::emax ? F::make(0, 0, neg, 2) : F::make(kept, ex, neg, 0);
 }
 
-
-// float value of an unsigned integer below 2^46 (the limb sums), rounded to
-// nearest, using only integer and FP32 adds: three 16-bit pieces, each made
-// exact by the 2^23 bit-pattern trick.
-__device__ __forceinline__ float u44_to_float(uint64_t y) {
-  const float a = __uint_as_float(0x4B000000u | (uint32_t)(y & 0xFFFF)) - 8388608.0f;
-  const float b = __uint_as_float(0x4B000000u | (uint32_t)((y >> 16) & 0xFFFF)) - 8388608.0f;
-  const float c = __uint_as_float(0x4B000000u | (uint32_t)(y >> 32)) - 8388608.0f;
-  return fmaf(c, 4294967296.0f, fmaf(b, 65536.0f, a));
-}
-
-__device__ __forceinline__ void store4(double *p, double a, double b, double c, double d) {
-  reinterpret_cast<double2 *>(p)[0] = make_double2(a, b);
-  reinterpret_cast<double2 *>(p)[1] = make_double2(c, d);
-}
-__device__ __forceinline__ void store4(float *p, float a, float b, float c, float d) {
-  *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
-}
-
-// Multiword add / subtract with the hardware carry chain (L <= 6 limbs,
-// modulo 2^(32 L)): s += a, s -= a.
-template <int L>
-__device__ __forceinline__ void add_chain(uint32_t (&s)[L], const uint32_t (&a)[L]) {
-  static_assert(L >= 2 && L <= 6, "2..6 limbs");
-  if constexpr (L == 2)
-    asm("add.cc.u32 %0, %0, %2;\n\taddc.u32 %1, %1, %3;" : "+r"(s[0]), "+r"(s[1]) : "r"(a[0]), "r"(a[1]));
-  else if constexpr (L == 3)
-    asm("add.cc.u32 %0, %0, %3;\n\taddc.cc.u32 %1, %1, %4;\n\taddc.u32 %2, %2, %5;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]) : "r"(a[0]), "r"(a[1]), "r"(a[2]));
-  else if constexpr (L == 4)
-    asm("add.cc.u32 %0, %0, %4;\n\taddc.cc.u32 %1, %1, %5;\n\taddc.cc.u32 %2, %2, %6;\n\t"
-        "addc.u32 %3, %3, %7;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]) : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]));
-  else if constexpr (L == 5)
-    asm("add.cc.u32 %0, %0, %5;\n\taddc.cc.u32 %1, %1, %6;\n\taddc.cc.u32 %2, %2, %7;\n\t"
-        "addc.cc.u32 %3, %3, %8;\n\taddc.u32 %4, %4, %9;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]));
-  else
-    asm("add.cc.u32 %0, %0, %6;\n\taddc.cc.u32 %1, %1, %7;\n\taddc.cc.u32 %2, %2, %8;\n\t"
-        "addc.cc.u32 %3, %3, %9;\n\taddc.cc.u32 %4, %4, %10;\n\taddc.u32 %5, %5, %11;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]));
-}
-template <int L>
-__device__ __forceinline__ void sub_chain(uint32_t (&s)[L], const uint32_t (&a)[L]) {
-  static_assert(L >= 2 && L <= 6, "2..6 limbs");
-  if constexpr (L == 2)
-    asm("sub.cc.u32 %0, %0, %2;\n\tsubc.u32 %1, %1, %3;" : "+r"(s[0]), "+r"(s[1]) : "r"(a[0]), "r"(a[1]));
-  else if constexpr (L == 3)
-    asm("sub.cc.u32 %0, %0, %3;\n\tsubc.cc.u32 %1, %1, %4;\n\tsubc.u32 %2, %2, %5;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]) : "r"(a[0]), "r"(a[1]), "r"(a[2]));
-  else if constexpr (L == 4)
-    asm("sub.cc.u32 %0, %0, %4;\n\tsubc.cc.u32 %1, %1, %5;\n\tsubc.cc.u32 %2, %2, %6;\n\t"
-        "subc.u32 %3, %3, %7;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]) : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]));
-  else if constexpr (L == 5)
-    asm("sub.cc.u32 %0, %0, %5;\n\tsubc.cc.u32 %1, %1, %6;\n\tsubc.cc.u32 %2, %2, %7;\n\t"
-        "subc.cc.u32 %3, %3, %8;\n\tsubc.u32 %4, %4, %9;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]));
-  else
-    asm("sub.cc.u32 %0, %0, %6;\n\tsubc.cc.u32 %1, %1, %7;\n\tsubc.cc.u32 %2, %2, %8;\n\t"
-        "subc.cc.u32 %3, %3, %9;\n\tsubc.cc.u32 %4, %4, %10;\n\tsubc.u32 %5, %5, %11;"
-        : "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]));
-}
-
 template <int N, typename OutT>
 __global__ void __launch_bounds__(kThreads)
     k_crt(int m, int n, int groups, const int8_t *__restrict__ c, int ldcres,
@@ -257,7 +189,6 @@ __global__ void __launch_bounds__(kThreads)
   }
   const int ei = e[i];
 
-  OutT o0 = OutT(0), o1 = OutT(0), o2 = OutT(0), o3 = OutT(0);
 #pragma unroll 1
   for (int u = 0; u < 4; u++) {
     const int j = j0 + u;
@@ -273,32 +204,21 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int v = 0; v < LW; v++) Y[v] += (uint64_t)cl * cc.W32[l][v];
     }
-    // q = round((Y - K) / P) from the two top limb sums (converted without the
-    // conversion or FP64 units: see u44_to_float)
-    float t = fmaf(u44_to_float(Y[LW - 1]), cc.s_top, -cc.KoverP);
-    if (LW > 1) t = fmaf(u44_to_float(Y[LW > 1 ? LW - 2 : 0]), cc.s_next, t);
-    const float tq = t + 12582912.0f;  // 1.5 * 2^23: rounds t to an integer (|t| < 2^22)
-    const float qf = tq - 12582912.0f;
-    // X = Y - K - q P = Y + NK - q' P with q' = q + 4096 >= 0 (|q| <= 128 N)
-    // and NK = -(K - 4096 P) (two's complement), all in carry chains.
-    const uint32_t qq = (uint32_t)(__float_as_int(tq) - 0x4B400000 + 4096);
-    uint32_t x[LX], hi[LX], pl[LX], ph[LX];
+    // q = round((Y - K) / P) from the two top limb sums
+    float t = (float)Y[LW - 1] * cc.s_top - cc.KoverP;
+    if (LW > 1) t = fmaf((float)Y[LW > 1 ? LW - 2 : 0], cc.s_next, t);
+    const float qf = rintf(t);
+    const int q = (int)qf;
+    // X = Y - K - q P in signed 64-bit limb sums, then one carry pass
+    uint32_t x[LX];
+    long long carry = 0;
 #pragma unroll
     for (int v = 0; v < LX; v++) {
-      x[v] = v < LW ? (uint32_t)Y[v < LW ? v : 0] : 0u;
-      hi[v] = (v >= 1 && v - 1 < LW) ? (uint32_t)(Y[v >= 1 && v - 1 < LW ? v - 1 : 0] >> 32) : 0u;
-      const uint32_t pv = v < LW ? cc.P32[v < LW ? v : 0] : 0u;
-      const uint32_t pp = (v >= 1 && v - 1 < LW) ? cc.P32[v >= 1 && v - 1 < LW ? v - 1 : 0] : 0u;
-      pl[v] = qq * pv;
-      ph[v] = __umulhi(qq, pp);
+      const long long yv = v < LW ? (long long)Y[v < LW ? v : 0] : 0ll;
+      const long long sv = yv - (long long)cc.K32[v] - (long long)q * (long long)cc.P32[v] + carry;
+      x[v] = (uint32_t)sv;
+      carry = sv >> 32;
     }
-    uint32_t nk[LX];
-#pragma unroll
-    for (int v = 0; v < LX; v++) nk[v] = cc.NK32[v];
-    add_chain<LX>(x, hi);
-    add_chain<LX>(x, nk);
-    sub_chain<LX>(x, pl);
-    sub_chain<LX>(x, ph);
     // X is far inside the 32*LX-bit window, so its sign is the top bit of
     // x[LX-1].  The quotient can be off by one only when the estimate sat
     // within 0.01 of a half-integer; then compare X with +-P/2 exactly.
@@ -345,21 +265,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int v = 0; v < LX; v++) mag[v] = x[v];
     }
-    const OutT r = round_scaled_fast<OutT, LX>(mag, neg, ei + f[j]);
-    if (u == 0) o0 = r;
-    else if (u == 1) o1 = r;
-    else if (u == 2) o2 = r;
-    else o3 = r;
-  }
-  // the warp's 32 x 4 consecutive results leave as whole vectors when aligned
-  OutT *crow = C + (size_t)i * ldc + j0;
-  if (j0 + 4 <= n && (reinterpret_cast<uintptr_t>(crow) % (4 * sizeof(OutT))) == 0) {
-    store4(crow, o0, o1, o2, o3);
-  } else {
-    if (j0 < n) crow[0] = o0;
-    if (j0 + 1 < n) crow[1] = o1;
-    if (j0 + 2 < n) crow[2] = o2;
-    if (j0 + 3 < n) crow[3] = o3;
+    C[(size_t)i * ldc + j] = round_scaled_fast<OutT, LX>(mag, neg, ei + f[j]);
   }
   }
 }

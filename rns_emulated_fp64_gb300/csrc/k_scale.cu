@@ -227,8 +227,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int u = 0; u < 8; u++) {
         const int h = h0 + u;
         const Dec d = decode(h < k ? __ldg(x + h) : T(0));
-        const uint32_t bar = (uint32_t)ceil_shift(d.mant, d.ex2 + 6 - E);  // 0..64
-        v[u] = __float2half_rn(__uint_as_float(0x4B000000u | bar) - 8388608.0f);
+        v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
       }
       *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
     }
@@ -296,11 +295,8 @@ __device__ __forceinline__ float residue_odd(const float (&w)[7], const ResConst
   return fmaf(-c.p[l], q, x);
 }
 
-// Signed value of a byte, as an exact float in [-128, 127], without a
-// conversion instruction (those share GB300's narrow FP64 pipe): the bit
-// pattern 0x4B000000 | u is the float 2^23 + u.
 __device__ __forceinline__ float byte_residue(uint32_t b) {
-  return __uint_as_float(0x4B000000u | (b ^ 0x80u)) - 8388736.0f;  // 2^23 + 128
+  return (float)((int)(b ^ 0x80u) - 128);  // [-128, 127]
 }
 
 template <int N, int NW, int EPT>

@@ -87,16 +87,6 @@ int u_bitlen(const U256 &a) {
     if (a.w[i]) return 32 * i + 32 - __builtin_clz(a.w[i]);
   return 0;
 }
-U256 u_sub(const U256 &a, const U256 &b) {  // modulo 2^256
-  U256 r;
-  int64_t br = 0;
-  for (int i = 0; i < 8; i++) {
-    int64_t d = (int64_t)a.w[i] - b.w[i] - br;
-    br = d < 0;
-    r.w[i] = (uint32_t)d;
-  }
-  return r;
-}
 U256 u_add(const U256 &a, const U256 &b) {
   U256 r;
   uint64_t c = 0;
@@ -163,12 +153,10 @@ void build_tables(int N, Os2Tables *t) {
     Ksum = u_add(Ksum, W);
   }
   const U256 K = u_mul(Ksum, 128);
-  const U256 NK = u_sub(u_mul(P, 4096), K);
   for (int v = 0; v < 6; v++) {
     t->crt.P32[v] = P.w[v];
     t->crt.K32[v] = K.w[v];
     t->crt.H32[v] = half.w[v];
-    t->crt.NK32[v] = NK.w[v];
   }
   const int LW = (N + 3) / 4;
   const double Pd = u_to_double(P);

@@ -31,7 +31,6 @@ struct CrtConsts {
   uint32_t P32[6];                   // P
   uint32_t K32[6];                   // K = 128 sum_l W_l (offset of the unsigned residues)
   uint32_t H32[6];                   // P / 2
-  uint32_t NK32[6];                  // 4096 P - K modulo 2^192 (offset quotient q + 4096)
   float s_top, s_next;               // fl(2^(32(LW-1)) / P), fl(2^(32(LW-2)) / P), LW = (N+3)/4
   float KoverP;                      // fl(K / P)
 };
