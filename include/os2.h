@@ -128,9 +128,18 @@ os2_status os2_cgemm(int m, int n, int k, const float *A, int lda, const float *
 size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode);
 
 /* End-to-end variant of os2_gemm whose A, B, C are HOST pointers (pinned
- * memory gives asynchronous copies).  Enqueues the host-to-device copies of A
- * and B, the five steps, and the device-to-host copy of C on `stream`; the
- * caller synchronises the stream before reading C. */
+ * memory gives asynchronous copies; pageable memory works, with copies that
+ * block the calling thread).  Results are identical to os2_gemm's.  The copies
+ * overlap the kernels: A and B travel in panels (row panels of A, column
+ * panels of B, about 2048 rows each) on a library-owned copy-in stream, each
+ * block of C is computed on `stream` once its two panels have arrived, and
+ * leaves on a library-owned copy-out stream while the next block is computed.
+ * Both copy streams (created once per device, non-blocking) first wait for
+ * the work already enqueued on `stream`, and `stream` waits for the last copy
+ * out, so synchronising `stream` covers the whole call; the caller
+ * synchronises it before reading C, and must not reuse the workspace on
+ * another stream before then.  Calls from several host threads are enqueued
+ * one at a time. */
 os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
                          double *C, int ldc, int num_moduli, int mode, void *workspace,
                          size_t workspace_bytes, void *stream);

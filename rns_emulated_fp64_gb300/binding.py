@@ -127,7 +127,8 @@ def _ptr(t) -> int | None:
 
 def _kmat(X, name):
     """float64 CUDA matrix whose rows are contiguous; returns (X, ld)."""
-    if not (X.is_cuda and X.dtype == torch.float64 and X.dim() == 2 and X.stride(1) == 1):
+    if not (X.is_cuda and X.dtype == torch.float64 and X.dim() == 2 and
+            (X.stride(1) == 1 or X.shape[1] <= 1)):
         raise ValueError(f"{name} must be a 2-D float64 CUDA tensor with contiguous rows")
     return X, max(X.stride(0), max(X.shape[1], 1))
 
@@ -254,7 +255,8 @@ def gemm_host(A, Bt, C, num_moduli=14, mode="fast", workspace=None, stream=None)
     """End-to-end call on HOST tensors (pinned for asynchronous copies): copies
     in, five steps, copy out, all enqueued on `stream`; synchronise before use."""
     for X, nm in ((A, "A"), (Bt, "Bt"), (C, "C")):
-        if X.is_cuda or X.dtype != torch.float64 or X.dim() != 2 or X.stride(1) != 1:
+        if X.is_cuda or X.dtype != torch.float64 or X.dim() != 2 or (
+                X.stride(1) != 1 and X.shape[1] > 1):
             raise ValueError(f"{nm} must be a 2-D float64 host tensor with contiguous rows")
     m, k = A.shape
     n = Bt.shape[0]

@@ -631,12 +631,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// FP16 planes [nplanes][rows][kp]; box = 64 (k) x box_rows x 1, 128-byte swizzle.
-bool make_map(CUtensorMap *map, const void *base, int kp, int rows, int nplanes, int box_rows) {
+// FP16 planes [nplanes][plane_rows][kp], of which the first `rows` rows are
+// mapped; box = 64 (k) x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap *map, const void *base, int kp, int rows, int nplanes, int box_rows,
+              int plane_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kp, (cuuint64_t)rows, (cuuint64_t)nplanes};
-  cuuint64_t strides[2] = {(cuuint64_t)kp * 2, (cuuint64_t)kp * 2 * (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kp * 2, (cuuint64_t)kp * 2 * (cuuint64_t)plane_rows};
   cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims,
@@ -655,7 +657,7 @@ int num_sms() {
 template <int KIND>
 cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
                    int ldo, int32_t *rowmax, int32_t *colmax, int prod_bound_log2,
-                   const Os2Tables *t, int *status, cudaStream_t s) {
+                   const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows) {
   using C = Cfg<KIND>;
   constexpr size_t smem = 1024 + (size_t)C::STAGES * (BM + C::BN) * BK * 2 + 256;
   static std::once_flag once;
@@ -666,7 +668,8 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, RA, kp, m, nplanes, BM) || !make_map(&mb, RB, kp, n, nplanes, C::BN))
+  if (!make_map(&ma, RA, kp, m, nplanes, BM, m) ||
+      !make_map(&mb, RB, kp, n, nplanes, C::BN, b_plane_rows))
     return cudaErrorInvalidValue;
   Sched sp;
   sp.m = m;
@@ -691,7 +694,7 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
 }
 
 cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
-                    int ldo, const Os2Tables *t, int *status, cudaStream_t s) {
+                    int ldo, const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows) {
   constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -701,7 +704,8 @@ cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int np
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, RA, kp, m, nplanes, kHalf) || !make_map(&mb, RB, kp, n, nplanes, kHalf))
+  if (!make_map(&ma, RA, kp, m, nplanes, kHalf, m) ||
+      !make_map(&mb, RB, kp, n, nplanes, kHalf, b_plane_rows))
     return cudaErrorInvalidValue;
   Sched sp;
   sp.m = m;
@@ -725,12 +729,15 @@ cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int np
 
 cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
                            int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,
-                           int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s) {
+                           int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s,
+                           int b_plane_rows) {
   if (m <= 0 || n <= 0 || kp <= 0) return cudaSuccess;
-  if (kind == 2) return launch2(m, n, kp, RA, RB, nplanes, out, ldo, t, status, s);
+  if (b_plane_rows <= 0) b_plane_rows = n;
+  if (b_plane_rows < n) return cudaErrorInvalidValue;
+  if (kind == 2) return launch2(m, n, kp, RA, RB, nplanes, out, ldo, t, status, s, b_plane_rows);
   if (kind == 0)
     return launch<0>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
-                     status, s);
+                     status, s, b_plane_rows);
   return launch<1>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
-                   status, s);
+                   status, s, b_plane_rows);
 }

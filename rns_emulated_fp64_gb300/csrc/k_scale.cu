@@ -172,7 +172,9 @@ struct RowSet {
   int rows;
   int32_t *e;       // exponents (out for scale, in for residues)
   int32_t *E;       // accurate mode: exponent bounds (out)
-  __half *planes;   // residue planes [N][rows][kp] or the magnitude plane [rows][kp]
+  __half *planes;   // residue planes [N][prow][kp] (first `rows` rows written) or the
+                    // magnitude plane [rows][kp]
+  long prow;        // rows from one residue plane to the next (>= rows)
 };
 
 // ------------------------------------------------------------- row scale ---
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int row = isA ? rr : rr - a.rows;
     const T *x = reinterpret_cast<const T *>(rs.X) + (size_t)row * rs.ldx;
     const int ee = __ldg(rs.e + row);
-    const size_t pstride = (size_t)rs.rows * kp;
+    const size_t pstride = (size_t)rs.prow * kp;
     const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
     for (int ch = blockIdx.x * kThreads + threadIdx.x; ch < cpr; ch += gridDim.x * kThreads) {
       const int h0 = ch * EPT;
@@ -393,8 +395,8 @@ cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int r
                              int rowsB, int32_t *eB, int32_t *EB, void *barsB, int k, int kp,
                              const Os2Tables *t, int *status, cudaStream_t s) {
   if (rowsA + rowsB <= 0) return cudaSuccess;
-  RowSet a{XA, lda, rowsA, eA, EA, reinterpret_cast<__half *>(barsA)};
-  RowSet b{XB, ldb, rowsB, eB, EB, reinterpret_cast<__half *>(barsB)};
+  RowSet a{XA, lda, rowsA, eA, EA, reinterpret_cast<__half *>(barsA), rowsA};
+  RowSet b{XB, ldb, rowsB, eB, EB, reinterpret_cast<__half *>(barsB), rowsB};
   dim3 grid(rowsA + rowsB);
   if (mode == SM_BARS) {
     if (f32) k_row_scale<SM_BARS, float><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
@@ -430,10 +432,12 @@ cudaError_t residues_t(const RowSet &a, const RowSet &b, int k, int kp, const Os
 cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const int32_t *eA,
                             void *planesA, const void *XB, long ldb, int rowsB,
                             const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
-                            cudaStream_t s) {
+                            cudaStream_t s, long prowB) {
   if (rowsA + rowsB <= 0 || kp <= 0) return cudaSuccess;
-  RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA)};
-  RowSet b{XB, ldb, rowsB, const_cast<int32_t *>(eB), nullptr, reinterpret_cast<__half *>(planesB)};
+  RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA),
+           rowsA};
+  RowSet b{XB, ldb, rowsB, const_cast<int32_t *>(eB), nullptr, reinterpret_cast<__half *>(planesB),
+           prowB > 0 ? prowB : rowsB};
   return f32 ? residues_t<float>(a, b, k, kp, t, s) : residues_t<double>(a, b, k, kp, t, s);
 }
 

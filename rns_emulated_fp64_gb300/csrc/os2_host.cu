@@ -282,6 +282,48 @@ os2_status check_gemm_args(int m, int n, int k, const void *A, int lda, const vo
   return OS2_OK;
 }
 
+// Step 1 in accurate mode: magnitude planes (aliasing the residue planes), one
+// exact bound product with fused row/column maxima, then the exponents e, f.
+os2_status accurate_exponents(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
+                              int ldb, void *ws, const Layout &L, const Os2Tables *t, int *status,
+                              cudaStream_t s) {
+  int32_t *e = at<int32_t>(ws, L.e), *f = at<int32_t>(ws, L.f);
+  void *pa = at<void>(ws, L.planesA), *pb = at<void>(ws, L.planesB);
+  int32_t *EA = at<int32_t>(ws, L.EA), *EB = at<int32_t>(ws, L.EB);
+  int32_t *R = at<int32_t>(ws, L.R), *K = at<int32_t>(ws, L.K);
+  cudaError_t err;
+  {
+    ProfScope ps("scale_bars", s);
+    if ((err = launch_row_scale(SM_BARS, f32, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB,
+                                pb, k, L.kp, t, status, s)))
+      return cuda_status(err);
+  }
+  if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
+  if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
+  {
+    ProfScope ps("gemm_bound", s);
+    if ((err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
+      return cuda_status(err);
+  }
+  if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
+  return cuda_status(launch_accu_exponents(K, EB, n, f, t, s));
+}
+
+// Step 3 for an m x n block: A planes [N][m][kp] and B planes [N][n][kp] give
+// the mod-p products [N][m][ldcres].
+os2_status residue_products(int m, int n, const Layout &L, const void *pa, const void *pb, int N,
+                            int8_t *cres, const Os2Tables *t, int *status, cudaStream_t s) {
+  ProfScope ps("gemm_modp", s);
+  const int variant = g_variant.load();
+  cudaError_t err;
+  if (variant == OS2_GEMM_SIMT)
+    err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
+  else
+    err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : 2, m, n, L.kp, pa, pb, N, cres,
+                         L.ldcres, nullptr, nullptr, 14, t, status, s);
+  return cuda_status(err);
+}
+
 // The five steps on device operands; arguments already checked.  f32: float
 // operands and result (SGEMM emulation), else double.
 os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const void *B, int ldb,
@@ -303,25 +345,8 @@ os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const
                                 nullptr, nullptr, k, L.kp, t, status, s)))
       return cuda_status(err);
   } else {
-    // step 1, accurate: magnitude planes (aliasing the residue planes), one
-    // exact bound product with fused row/column maxima, exponents
-    int32_t *EA = at<int32_t>(ws, L.EA), *EB = at<int32_t>(ws, L.EB);
-    int32_t *R = at<int32_t>(ws, L.R), *K = at<int32_t>(ws, L.K);
-    {
-      ProfScope ps("scale_bars", s);
-      if ((err = launch_row_scale(SM_BARS, f32, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB,
-                                  pb, k, L.kp, t, status, s)))
-        return cuda_status(err);
-    }
-    if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
-    if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
-    {
-      ProfScope ps("gemm_bound", s);
-      if ((err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
-        return cuda_status(err);
-    }
-    if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
-    if ((err = launch_accu_exponents(K, EB, n, f, t, s))) return cuda_status(err);
+    os2_status st = accurate_exponents(f32, m, n, k, A, lda, B, ldb, ws, L, t, status, s);
+    if (st) return st;
   }
   // step 2: residue planes of A and B
   {
@@ -330,16 +355,8 @@ os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const
       return cuda_status(err);
   }
   // step 3
-  {
-    ProfScope ps("gemm_modp", s);
-    const int variant = g_variant.load();
-    if (variant == OS2_GEMM_SIMT)
-      err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
-    else
-      err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : 2, m, n, L.kp, pa, pb, N, cres,
-                           L.ldcres, nullptr, nullptr, 14, t, status, s);
-    if (err) return cuda_status(err);
-  }
+  os2_status st = residue_products(m, n, L, pa, pb, N, cres, t, status, s);
+  if (st) return st;
   // steps 4 + 5
   ProfScope ps("crt_unscale", s);
   return cuda_status(launch_crt(f32, m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
@@ -465,6 +482,66 @@ static cudaError_t copy_rows(double *dst, size_t dpitch, const double *src, size
   return cudaMemcpy2DAsync(dst, 8 * dpitch, src, 8 * spitch, 8 * cols, rows, kind, s);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Host entry point pipeline.  Row panel i of C needs A's row panel i and all
+// of B; a block (row panel, column panel) needs only the two panels.  The
+// operands travel on a copy-in stream in the order A_0, B_0 .. B_{Q-1}, A_1 ..
+// A_{P-1}; the caller's stream scales, splits, multiplies and reconstructs
+// each block as soon as its panels have arrived, while later panels are still
+// in transit; each finished block of C leaves on a copy-out stream while the
+// next block's product runs.  The first and last row panels go block by block
+// (a short head before the first product, a short tail after the last); the
+// middle row panels go whole.  Accurate mode's exponents need all of A and all
+// of B, so there the compute waits for every panel; C still leaves by blocks.
+constexpr int kMaxPanels = 8;
+constexpr int kPanelMinRows = 2048;
+
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, out_done = nullptr;
+  cudaEvent_t a_in[kMaxPanels] = {}, b_in[kMaxPanels] = {}, c_done[3 * kMaxPanels] = {};
+  bool ready = false;
+};
+
+std::mutex g_host_mu;  // held while a call enqueues (its events are shared)
+
+// Streams and events of the pipeline on the current device, created once.
+HostPipe *host_pipe() {
+  static HostPipe pipes[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  HostPipe &p = pipes[dev];
+  if (p.ready) return &p;
+  bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess;
+  auto ev = [&](cudaEvent_t *x) {
+    ok = ok && cudaEventCreateWithFlags(x, cudaEventDisableTiming) == cudaSuccess;
+  };
+  ev(&p.start);
+  ev(&p.out_done);
+  for (int i = 0; i < kMaxPanels; i++) {
+    ev(&p.a_in[i]);
+    ev(&p.b_in[i]);
+  }
+  for (int i = 0; i < 3 * kMaxPanels; i++) ev(&p.c_done[i]);
+  p.ready = ok;
+  return ok ? &p : nullptr;
+}
+
+// Panel size along one dimension: at least kPanelMinRows, a multiple of the
+// 256-row tile of step 3, at most kMaxPanels panels.
+int panel_size(int rows) {
+  const int P = std::min(kMaxPanels, std::max(1, rows / kPanelMinRows));
+  return (int)os2_round_up((size_t)((rows + P - 1) / P), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
 os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
                          double *C, int ldc, int num_moduli, int mode, void *workspace,
                          size_t workspace_bytes, void *stream) {
@@ -480,15 +557,138 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
   double *dB = at<double>(workspace, L.total + os2_round_up(8 * (size_t)m * k, 256));
   double *dC = at<double>(workspace, L.total + os2_round_up(8 * (size_t)m * k, 256) +
                                           os2_round_up(8 * (size_t)n * k, 256));
-  const int kk = std::max(k, 1);
   cudaError_t err;
-  // The host link (about 210 GB/s each way here) bounds this call: the GEMM
-  // needs both operands complete, so the copies stay in order on `stream`.
-  if ((err = copy_rows(dA, kk, A, lda, k, m, cudaMemcpyHostToDevice, s))) return cuda_status(err);
-  if ((err = copy_rows(dB, kk, B, ldb, k, n, cudaMemcpyHostToDevice, s))) return cuda_status(err);
-  st = run_gemm(false, m, n, k, dA, kk, dB, kk, dC, n, num_moduli, mode, workspace, L, s);
-  if (st) return st;
-  return cuda_status(copy_rows(C, ldc, dC, n, n, m, cudaMemcpyDeviceToHost, s));
+  if (k == 0) {
+    if ((err = cudaMemsetAsync(dC, 0, 8 * (size_t)m * n, s))) return cuda_status(err);
+    return cuda_status(copy_rows(C, ldc, dC, n, n, m, cudaMemcpyDeviceToHost, s));
+  }
+  const int N = num_moduli;
+  const Os2Tables *t = os2_tables(N);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_host_mu);
+  HostPipe *p = host_pipe();
+  if (!p) return OS2_ERR_CUDA;
+  const int mp = panel_size(m), P = (m + mp - 1) / mp;
+  // column panels of B (the tensor-core step 3 reads a panel of B's planes in
+  // place; the CUDA-core reference variant takes B whole)
+  const int nq = g_variant.load() == OS2_GEMM_SIMT ? n : panel_size(n), Q = (n + nq - 1) / nq;
+  int32_t *e = at<int32_t>(workspace, L.e), *f = at<int32_t>(workspace, L.f);
+  char *pa = at<char>(workspace, L.planesA), *pb = at<char>(workspace, L.planesB);
+  int8_t *cres = at<int8_t>(workspace, L.cres);
+  const size_t plane_row = (size_t)L.kp * 2;  // bytes of one row of a plane
+#define OS2_TRY(x)                                           \
+  do {                                                       \
+    if ((err = (x)) != cudaSuccess) return cuda_status(err); \
+  } while (0)
+  // both copy streams start after the work already enqueued on `stream`
+  OS2_TRY(cudaEventRecord(p->start, s));
+  OS2_TRY(cudaStreamWaitEvent(p->in, p->start, 0));
+  OS2_TRY(cudaStreamWaitEvent(p->out, p->start, 0));
+  auto send_a = [&](int i) {
+    const int r0 = i * mp, mi = std::min(mp, m - r0);
+    cudaError_t r = copy_rows(dA + (size_t)r0 * k, k, A + (size_t)r0 * lda, lda, k, mi,
+                              cudaMemcpyHostToDevice, p->in);
+    return r ? r : cudaEventRecord(p->a_in[i], p->in);
+  };
+  OS2_TRY(send_a(0));
+  for (int j = 0; j < Q; j++) {
+    const int c0 = j * nq, nj = std::min(nq, n - c0);
+    OS2_TRY(copy_rows(dB + (size_t)c0 * k, k, B + (size_t)c0 * ldb, ldb, k, nj,
+                      cudaMemcpyHostToDevice, p->in));
+    OS2_TRY(cudaEventRecord(p->b_in[j], p->in));
+  }
+  for (int i = 1; i < P; i++) OS2_TRY(send_a(i));
+
+  // steps 1 + 2 for row panel i of A (fast mode: the panel's exponents too);
+  // the panel's planes are laid out as an mi-row problem
+  auto split_a = [&](int i) {
+    const int r0 = i * mp, mi = std::min(mp, m - r0);
+    const double *Ai = dA + (size_t)r0 * k;
+    cudaError_t r = cudaSuccess;
+    if (mode == OS2_MODE_FAST) {
+      if ((r = cudaStreamWaitEvent(s, p->a_in[i], 0))) return r;
+      ProfScope ps("scale", s);
+      r = launch_row_scale(SM_FAST_SCALE, false, Ai, k, mi, e + r0, nullptr, nullptr, nullptr, 0,
+                           0, nullptr, nullptr, nullptr, k, L.kp, t, status, s);
+      if (r) return r;
+    }
+    ProfScope ps("residues", s);
+    return launch_residues(false, Ai, k, mi, e + r0, pa + (size_t)r0 * N * plane_row, nullptr, 0,
+                           0, nullptr, nullptr, k, L.kp, t, s);
+  };
+  // steps 1 + 2 for column panel j of B, in place in B's [N][n][kp] planes
+  auto split_b = [&](int j) {
+    const int c0 = j * nq, nj = std::min(nq, n - c0);
+    const double *Bj = dB + (size_t)c0 * k;
+    cudaError_t r = cudaSuccess;
+    if (mode == OS2_MODE_FAST) {
+      if ((r = cudaStreamWaitEvent(s, p->b_in[j], 0))) return r;
+      ProfScope ps("scale", s);
+      r = launch_row_scale(SM_FAST_SCALE, false, nullptr, 0, 0, nullptr, nullptr, nullptr, Bj, k,
+                           nj, f + c0, nullptr, nullptr, k, L.kp, t, status, s);
+      if (r) return r;
+    }
+    ProfScope ps("residues", s);
+    return launch_residues(false, nullptr, 0, 0, nullptr, nullptr, Bj, k, nj, f + c0,
+                           pb + (size_t)c0 * plane_row, k, L.kp, t, s, n);
+  };
+  // steps 3-5 for the block (row panel i, columns c0 .. c0+nj), then its copy out
+  int blocks = 0;
+  auto block = [&](int i, int c0, int nj) -> os2_status {
+    const int r0 = i * mp, mi = std::min(mp, m - r0);
+    const void *pai = pa + (size_t)r0 * N * plane_row;
+    int8_t *ci = cres + (size_t)r0 * N * L.ldcres + c0;
+    const char *pbj = pb + (size_t)c0 * plane_row;
+    {
+      ProfScope ps("gemm_modp", s);
+      const int variant = g_variant.load();
+      if (variant == OS2_GEMM_SIMT)
+        err = launch_gemm_simt(mi, nj, L.kp, pai, pbj, N, OS2_OUT_MODP_INT8, ci, L.ldcres, t, s);
+      else
+        err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : 2, mi, nj, L.kp, pai, pbj, N, ci,
+                             L.ldcres, nullptr, nullptr, 14, t, status, s, n);
+      if (err) return cuda_status(err);
+    }
+    {
+      ProfScope ps("crt_unscale", s);
+      if ((err = launch_crt(false, mi, nj, ci, L.ldcres, e + r0, f + c0,
+                            dC + (size_t)r0 * n + c0, n, nullptr, t, s)))
+        return cuda_status(err);
+    }
+    cudaEvent_t done = p->c_done[blocks++];
+    if ((err = cudaEventRecord(done, s))) return cuda_status(err);
+    if ((err = cudaStreamWaitEvent(p->out, done, 0))) return cuda_status(err);
+    return cuda_status(copy_rows(C + (size_t)r0 * ldc + c0, ldc, dC + (size_t)r0 * n + c0, n, nj,
+                                 mi, cudaMemcpyDeviceToHost, p->out));
+  };
+  auto row_panel = [&](int i, bool by_blocks) -> os2_status {
+    if (!by_blocks) return block(i, 0, n);
+    for (int j = 0; j < Q; j++) {
+      const int c0 = j * nq;
+      if (i == 0) OS2_TRY(split_b(j));
+      if ((st = block(i, c0, std::min(nq, n - c0)))) return st;
+    }
+    return OS2_OK;
+  };
+
+  if (mode == OS2_MODE_ACCURATE) {
+    OS2_TRY(cudaStreamWaitEvent(s, p->b_in[Q - 1], 0));
+    OS2_TRY(cudaStreamWaitEvent(s, p->a_in[P - 1], 0));
+    if ((st = accurate_exponents(false, m, n, k, dA, k, dB, k, workspace, L, t, status, s)))
+      return st;
+  }
+  OS2_TRY(split_a(0));
+  if ((st = row_panel(0, true))) return st;
+  for (int i = 1; i < P; i++) {
+    OS2_TRY(split_a(i));
+    if ((st = row_panel(i, i == P - 1))) return st;
+  }
+  // `stream` covers everything: it waits for the last copy out
+  OS2_TRY(cudaEventRecord(p->out_done, p->out));
+  OS2_TRY(cudaStreamWaitEvent(s, p->out_done, 0));
+#undef OS2_TRY
+  return OS2_OK;
 }
 
 os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double *B, int ldb,

@@ -75,7 +75,7 @@ cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int r
 cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const int32_t *eA,
                             void *planesA, const void *XB, long ldb, int rowsB,
                             const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
-                            cudaStream_t s);
+                            cudaStream_t s, long prowB = 0);
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,
                                   const Os2Tables *t, cudaStream_t s);
 // f32: C is float (correctly rounded to binary32) instead of double.
@@ -90,7 +90,8 @@ cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *R
 // (14 for residues, 12 for the accurate-mode magnitude planes).
 cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
                            int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,
-                           int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s);
+                           int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s,
+                           int b_plane_rows = 0);
 
 // Complex products: interleaved complex operands <-> stacked real operands.
 cudaError_t launch_complex_stack(bool f32, int m, int n, int k, const void *A, long lda,

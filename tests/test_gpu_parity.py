@@ -326,10 +326,14 @@ def test_scale_invariance_on_gpu(s):
 
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
 @pytest.mark.parametrize("m,n,k,pinned", [(100, 120, 300, True), (1001, 700, 513, True),
-                                          (3, 2, 5, False)])
+                                          (3, 2, 5, False), (5000, 300, 200, True),
+                                          (9000, 72, 96, True), (4100, 33, 40, False),
+                                          (5, 4, 0, True)])
 def test_host_entry_point_matches_device(mode, m, n, k, pinned):
-    """The end-to-end host entry point (copies in, five steps, copy out; fast
-    mode pipelines the copies with the kernels) equals the device one."""
+    """The end-to-end host entry point (B in, then A in row panels that are
+    scaled, split, multiplied and reconstructed while later panels are still in
+    transit, C out by panels) equals the device one.  m >= 4096 gives several
+    panels, the last one ragged."""
     A, Bt = workloads.make_pair("spread", m, n, k, seed=6, phi=2.0)
     Ah = torch.from_numpy(A)
     Bh = torch.from_numpy(Bt)
@@ -341,6 +345,32 @@ def test_host_entry_point_matches_device(mode, m, n, k, pinned):
     status_ok()
     Cd = os2.gemm(dev(A), dev(Bt), 14, mode).cpu().numpy()
     assert_bits_equal(Ch.numpy(), Cd, "host vs device entry")
+
+
+def test_host_entry_point_strided_back_to_back():
+    """Row strides on all three host matrices, a side stream, and two calls in
+    a row on one workspace with one synchronisation at the end: the second
+    call's copies in wait for the first call's kernels."""
+    m, n, k = 4700, 260, 150
+    A1, B1 = workloads.make_pair("spread", m, n, k, seed=11, phi=1.0)
+    A2, B2 = workloads.make_pair("normal", m, n, k, seed=12)
+    big = lambda r, c: torch.full((r, c), np.nan, dtype=torch.float64).pin_memory()
+    Ah1, Bh1, Ah2, Bh2 = big(m, k + 9), big(n, k + 3), big(m, k + 9), big(n, k + 3)
+    Ah1[:, :k] = torch.from_numpy(A1)
+    Bh1[:, :k] = torch.from_numpy(B1)
+    Ah2[:, :k] = torch.from_numpy(A2)
+    Bh2[:, :k] = torch.from_numpy(B2)
+    Ch1, Ch2 = big(m, n + 5), big(m, n + 5)
+    ws = os2.alloc_workspace(os2.host_workspace_size(m, n, k, 16, "fast"))
+    side = torch.cuda.Stream()
+    os2.gemm_host(Ah1[:, :k], Bh1[:, :k], Ch1[:, :n], 16, "fast", workspace=ws, stream=side)
+    os2.gemm_host(Ah2[:, :k], Bh2[:, :k], Ch2[:, :n], 16, "fast", workspace=ws, stream=side)
+    side.synchronize()
+    status_ok()
+    for A, Bt, Ch in ((A1, B1, Ch1), (A2, B2, Ch2)):
+        Cd = os2.gemm(dev(A), dev(Bt), 16, "fast").cpu().numpy()
+        assert_bits_equal(Ch[:, :n].numpy(), Cd, "host vs device entry")
+        assert torch.isnan(Ch[:, n:]).all(), "wrote past the row of C"
 
 
 # ----------------------------------------------------- inner dimension >= 2^17 --
