@@ -77,6 +77,14 @@ __device__ __forceinline__ void job_coords(int job, const Sched &sp, int &l, int
   tn = w / rows_in;
 }
 
+// First k-block of chunk c: the kb_total k-blocks split into nchunks chunks
+// whose lengths differ by at most one (each <= sp.chunk, since nchunks =
+// ceil(kb_total / chunk)), so no chunk is much shorter than the epilogue work
+// that overlaps it.
+__device__ __forceinline__ int chunk_begin(const Sched &sp, int c) {
+  return (int)((long long)c * sp.kb_total / sp.nchunks);
+}
+
 // The unit sequence every role walks: (job, chunk, TMEM buffer).
 template <int KIND, typename F>
 __device__ __forceinline__ void for_each_unit_of(const Sched &sp, int b, int G, F &&f) {
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for_each_unit<KIND>(sp, [&](int job, int c, int) -> bool {
         int l, tm, tn;
         job_coords(job, sp, l, tm, tn);
-        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        const int kb0 = chunk_begin(sp, c), kb1 = chunk_begin(sp, c + 1);
         for (int kb = kb0; kb < kb1; kb++) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1, s_abort, kWaitLimit)) {
             *s_abort = 1;
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         aphase[buf] ^= 1;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        const int kb0 = chunk_begin(sp, c), kb1 = chunk_begin(sp, c + 1);
         for (int kb = kb0; kb < kb1; kb++) {
           if (!mbar_wait_bounded(&full[stage], phase, s_abort, kWaitLimit)) {
             *s_abort = 1;
@@ -459,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for_each_unit_of<0>(sp, pair, npairs, [&](int job, int c, int) -> bool {
         int l, tm, tn;
         job_coords(job, sp, l, tm, tn);
-        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        const int kb0 = chunk_begin(sp, c), kb1 = chunk_begin(sp, c + 1);
         for (int kb = kb0; kb < kb1; kb++) {
           if (!mbar_wait_cluster_bounded(&empty[stage], phase ^ 1, s_abort, kWaitLimit)) {
             *s_abort = 1;
@@ -503,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         aphase[buf] ^= 1;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-        const int kb0 = c * sp.chunk, kb1 = min(sp.kb_total, kb0 + sp.chunk);
+        const int kb0 = chunk_begin(sp, c), kb1 = chunk_begin(sp, c + 1);
         for (int kb = kb0; kb < kb1; kb++) {
           if (!mbar_wait_cluster_bounded(&full[stage], phase, s_abort, kWaitLimit)) {
             *s_abort = 1;
