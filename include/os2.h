@@ -183,6 +183,22 @@ int os2_moduli(int num_moduli, int32_t *out);
  * device and clears it. */
 os2_status os2_get_status(void *stream);
 
+/* Self-test of the device-side failure detection (the pages have no
+ * counterpart: it checks this library's own safeguard).  Every mbarrier wait
+ * of the tensor-core kernels gives up after a bounded number of clock cycles,
+ * or when its CTA's abort flag is raised, and then records OS2_ERR_TIMEOUT.
+ * This enqueues one CTA on `stream` whose wait on an mbarrier that nothing
+ * arrives at runs out after `limit_cycles` SM clock cycles
+ * (1 <= limit_cycles <= 2^34; 2e6 is about a millisecond).  The device status
+ * word then holds OS2_ERR_TIMEOUT (read and clear it with os2_get_status) and
+ * the context stays usable.  If `result` (caller-owned device memory, 8
+ * int32) is not NULL it receives: [0] 1 if a satisfied wait completed, [1] 1
+ * if the unsatisfied wait gave up, [2] the same for the cluster-scope wait,
+ * [3] 1 if a raised abort flag ended a wait early, [4] 1 if the timed-out
+ * wait lasted at least limit_cycles; [5..7] 0.  Returns OS2_ERR_INVALID_ARG
+ * for a limit out of range (nothing enqueued). */
+os2_status os2_wait_selftest(long long limit_cycles, int32_t *result, void *stream);
+
 /* Selects the step-3 kernel used by os2_gemm (process-wide; default TC). */
 os2_status os2_set_gemm_variant(int variant);
 

@@ -27,7 +27,7 @@ EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gem
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
            "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
            "os2_gemm_noalloc", "os2_sgemm", "os2_complex_workspace_size", "os2_zgemm",
-           "os2_cgemm")
+           "os2_cgemm", "os2_wait_selftest")
 
 _lib = None
 _lock = threading.Lock()
@@ -95,6 +95,8 @@ def load(build_if_missing: bool = True):
         L.os2_zgemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
         L.os2_zgemm.restype = i
         L.os2_cgemm.argtypes = [i, i, i, d, i, d, i, d, i, i, i, vp, sz, vp]
+        L.os2_wait_selftest.argtypes = [ct.c_longlong, vp, vp]
+        L.os2_wait_selftest.restype = i
         L.os2_cgemm.restype = i
         _lib = L
         return L
@@ -165,6 +167,16 @@ def set_gemm_variant(variant: int):
 def get_status(stream=None) -> int:
     return int(load().os2_get_status(_stream(stream)))
 
+
+def wait_selftest(limit_cycles: int = 2_000_000, stream=None) -> list[int]:
+    """Failure-detection self-test: one CTA whose bounded mbarrier waits run out
+    after `limit_cycles` clock cycles.  Returns the kernel's eight result words
+    (see os2_wait_selftest); the device status word is left at ERR_TIMEOUT."""
+    out = torch.zeros(8, dtype=torch.int32, device="cuda")
+    _check(load().os2_wait_selftest(int(limit_cycles), _ptr(out), _stream(stream)),
+           "os2_wait_selftest")
+    torch.cuda.synchronize()
+    return [int(v) for v in out.cpu()]
 
 def gemm(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int = 14, mode="fast", out=None,
          workspace=None, stream=None) -> torch.Tensor:

@@ -797,6 +797,14 @@ int os2_moduli(int num_moduli, int32_t *out) {
   return num_moduli;
 }
 
+os2_status os2_wait_selftest(long long limit_cycles, int32_t *result, void *stream) {
+  if (limit_cycles < 1 || limit_cycles > (1LL << 34)) return OS2_ERR_INVALID_ARG;
+  int *status = os2_status_ptr();
+  if (!status) return OS2_ERR_CUDA;
+  return cuda_status(
+      launch_wait_selftest(limit_cycles, status, result, static_cast<cudaStream_t>(stream)));
+}
+
 os2_status os2_get_status(void *stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return OS2_ERR_CUDA;

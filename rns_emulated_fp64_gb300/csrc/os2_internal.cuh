@@ -59,6 +59,9 @@ const Os2Tables *os2_tables(int N);
 // Per-device status word (device address), set up on first use.
 int *os2_status_ptr();
 
+// One CTA whose bounded mbarrier waits run out (failure-detection self-test).
+cudaError_t launch_wait_selftest(long long limit, int *status, int32_t *result, cudaStream_t s);
+
 // Row-scale kernel modes.
 enum ScaleMode {
   SM_FAST_SCALE = 0,   // fast mode: e_i from the revised bound

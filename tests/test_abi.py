@@ -90,6 +90,9 @@ def test_argument_errors_are_synchronous():
     c = lib.os2_crt
     assert c(4, 4, P, 2, 14, P, P, P, 4, None, None) == binding.ERR_INVALID_ARG     # ldcres < n
     assert lib.os2_set_gemm_variant(3) == binding.ERR_INVALID_ARG
+    w = lib.os2_wait_selftest
+    assert w(0, None, None) == binding.ERR_INVALID_ARG                 # limit < 1
+    assert w((1 << 34) + 1, None, None) == binding.ERR_INVALID_ARG     # limit > 2^34
 
 
 def test_binding_raises_without_fallback(monkeypatch):
