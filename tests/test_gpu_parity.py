@@ -298,6 +298,28 @@ def test_edge_cases():
         assert_bits_equal(Cg, ref.C, f"edge {mode}")
 
 
+@pytest.mark.parametrize("k", [1, 511, 1023, 1025, 2049, 4095, 8191, 8192, 8193])
+def test_odd_leading_dimensions(k):
+    """Rows that start off the 16-byte boundary (odd leading dimensions) take the
+    scalar-load paths of the scaling and residue kernels; k spans the sizes at
+    which the fast scaling holds a row in registers and the two-pass fallback."""
+    rng = np.random.default_rng(k)
+    m, n = 37, 29
+    Abig = rng.standard_normal((m, k + 1)) * np.exp2(rng.integers(-20, 20, size=(m, k + 1)))
+    Bbig = rng.standard_normal((n, k + 3))
+    A, Bt = Abig[:, :k], Bbig[:, :k]
+    for mode, om in (("fast", orc.FAST), ("accurate", orc.ACCURATE)):
+        Cg = os2.gemm(dev(Abig)[:, :k], dev(Bbig)[:, :k], 14, mode).cpu().numpy()
+        status_ok()
+        ref = orc.gemm_entries(np.ascontiguousarray(A), np.ascontiguousarray(Bt), 14, mode=om,
+                               want_X=False, want_c=False, want_G=False)
+        assert ref.mismatches == 0
+        assert_bits_equal(Cg, ref.C, f"odd ld, k={k}, {mode}")
+    e, f = os2.scale(dev(Abig)[:, :k], dev(Bbig)[:, :k], 14, "fast")
+    assert np.array_equal(e.cpu().numpy(), orc.scale_fast(np.ascontiguousarray(A), 14))
+    assert np.array_equal(f.cpu().numpy(), orc.scale_fast(np.ascontiguousarray(Bt), 14))
+
+
 def test_nonfinite_input_sets_status():
     A, Bt = workloads.make_pair("normal", 40, 40, 40)
     A[3, 4] = np.nan
