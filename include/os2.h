@@ -88,7 +88,13 @@ typedef enum {
 size_t os2_workspace_size(int m, int n, int k, int num_moduli, int mode);
 
 /* The whole five-step emulated DGEMM, C = A*B.  Layouts above.  Returns after
- * enqueueing on `stream`. */
+ * enqueueing on `stream`.  For m >= 4096 the rows of A go in panels of about
+ * 2048: the CRT and unscaling of one panel run on a library-owned stream
+ * (created once per device, non-blocking) beside the product of the next; that
+ * stream first waits for the work already on `stream`, and `stream` waits for
+ * it before the call's work ends, so synchronising `stream` covers the call.
+ * Results are identical either way.  Calls from several host threads are
+ * enqueued one at a time. */
 os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
                     double *C, int ldc, int num_moduli, int mode, void *workspace,
                     size_t workspace_bytes, void *stream);
@@ -132,9 +138,10 @@ size_t os2_host_workspace_size(int m, int n, int k, int num_moduli, int mode);
  * block the calling thread).  Results are identical to os2_gemm's.  The copies
  * overlap the kernels: A and B travel in panels (row panels of A, column
  * panels of B, about 2048 rows each) on a library-owned copy-in stream, each
- * block of C is computed on `stream` once its two panels have arrived, and
- * leaves on a library-owned copy-out stream while the next block is computed.
- * Both copy streams (created once per device, non-blocking) first wait for
+ * block of C is computed on `stream` once its two panels have arrived (its
+ * CRT on a library-owned stream beside the next block's product), and leaves
+ * on a library-owned copy-out stream while the next block is computed.  The
+ * library's streams (created once per device, non-blocking) first wait for
  * the work already enqueued on `stream`, and `stream` waits for the last copy
  * out, so synchronising `stream` covers the whole call; the caller
  * synchronises it before reading C, and must not reuse the workspace on

@@ -324,6 +324,17 @@ os2_status residue_products(int m, int n, const Layout &L, const void *pa, const
   return cuda_status(err);
 }
 
+// Panels of rows (of A) or columns (of B) for the pipelined paths.
+constexpr int kMaxPanels = 8;
+constexpr int kPanelMinRows = 2048;
+
+// Panel size along one dimension: at least kPanelMinRows, a multiple of the
+// 256-row tile of step 3, at most kMaxPanels panels.
+int panel_size(int rows) {
+  const int P = std::min(kMaxPanels, std::max(1, rows / kPanelMinRows));
+  return (int)os2_round_up((size_t)((rows + P - 1) / P), 256);
+}
+
 // The five steps on device operands; arguments already checked.  f32: float
 // operands and result (SGEMM emulation), else double.
 os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const void *B, int ldb,
@@ -362,6 +373,112 @@ os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const
   return cuda_status(launch_crt(f32, m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
 }
 
+// Device-path pipeline.  Step 3 fills every SM with one persistent CTA that
+// holds most of the shared memory but few threads and registers, so the CUDA
+// cores are nearly idle while it runs; a CRT CTA needs no shared memory and
+// fits beside it.  With A cut into row panels, the CRT and unscaling of panel
+// i-1 run on a side stream, on those idle units, while panel i is multiplied
+// on the caller's stream.  (Running the residues of the next panel beside the
+// product as well was measured no faster: they contend with it for memory.)
+struct DevPipe {
+  cudaStream_t crt = nullptr;
+  cudaEvent_t done = nullptr;
+  cudaEvent_t g_done[kMaxPanels] = {};
+  bool ready = false;
+};
+
+std::mutex g_dev_mu;  // held while a call enqueues (its events are shared)
+
+DevPipe *dev_pipe() {
+  static DevPipe pipes[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  DevPipe &p = pipes[dev];
+  if (p.ready) return &p;
+  bool ok = cudaStreamCreateWithFlags(&p.crt, cudaStreamNonBlocking) == cudaSuccess;
+  auto ev = [&](cudaEvent_t *x) {
+    ok = ok && cudaEventCreateWithFlags(x, cudaEventDisableTiming) == cudaSuccess;
+  };
+  ev(&p.done);
+  for (int i = 0; i < kMaxPanels; i++) ev(&p.g_done[i]);
+  p.ready = ok;
+  return ok ? &p : nullptr;
+}
+
+// The five steps with A in row panels (m, n, k > 0; arguments checked).  The
+// results are those of run_gemm: every entry goes through the same steps.
+os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
+                           int ldb, void *C, int ldc, int N, int mode, void *ws, const Layout &L,
+                           cudaStream_t s) {
+  const size_t es = f32 ? 4 : 8;
+  const Os2Tables *t = os2_tables(N);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  std::lock_guard<std::mutex> g(g_dev_mu);
+  DevPipe *p = dev_pipe();
+  if (!p) return OS2_ERR_CUDA;
+  const int mp = panel_size(m), P = (m + mp - 1) / mp;
+  int32_t *e = at<int32_t>(ws, L.e), *f = at<int32_t>(ws, L.f);
+  char *pa = at<char>(ws, L.planesA);
+  void *pb = at<void>(ws, L.planesB);
+  int8_t *cres = at<int8_t>(ws, L.cres);
+  const size_t plane_row = (size_t)L.kp * 2;
+  const char *Ab = static_cast<const char *>(A);
+  char *Cb = static_cast<char *>(C);
+  cudaError_t err;
+#define OS2_TRY(x)                                           \
+  do {                                                       \
+    if ((err = (x)) != cudaSuccess) return cuda_status(err); \
+  } while (0)
+  // step 1 on `stream`
+  if (mode == OS2_MODE_FAST) {
+    ProfScope ps("scale", s);
+    OS2_TRY(launch_row_scale(SM_FAST_SCALE, f32, A, lda, m, e, nullptr, nullptr, B, ldb, n, f,
+                             nullptr, nullptr, k, L.kp, t, status, s));
+  } else {
+    os2_status st = accurate_exponents(f32, m, n, k, A, lda, B, ldb, ws, L, t, status, s);
+    if (st) return st;
+  }
+  // step 2, row panel by row panel (each panel's planes laid out as an mi-row
+  // problem), B's with the first
+  {
+    ProfScope ps("residues", s);
+    for (int i = 0; i < P; i++) {
+      const int r0 = i * mp, mi = std::min(mp, m - r0);
+      OS2_TRY(launch_residues(f32, Ab + (size_t)r0 * lda * es, lda, mi, e + r0,
+                              pa + (size_t)r0 * N * plane_row, B, ldb, i == 0 ? n : 0, f, pb, k,
+                              L.kp, t, s));
+    }
+  }
+  // step 3 per panel on `stream`; steps 4 + 5 per panel on side stream 2
+  for (int i = 0; i < P; i++) {
+    const int r0 = i * mp, mi = std::min(mp, m - r0);
+    int8_t *ci = cres + (size_t)r0 * N * L.ldcres;
+    os2_status st =
+        residue_products(mi, n, L, pa + (size_t)r0 * N * plane_row, pb, N, ci, t, status, s);
+    if (st) return st;
+    OS2_TRY(cudaEventRecord(p->g_done[i], s));
+    OS2_TRY(cudaStreamWaitEvent(p->crt, p->g_done[i], 0));
+    ProfScope ps("crt_unscale", p->crt);
+    OS2_TRY(launch_crt(f32, mi, n, ci, L.ldcres, e + r0, f, Cb + (size_t)r0 * ldc * es, ldc,
+                       nullptr, t, p->crt));
+  }
+  // `stream` covers everything: it waits for the last reconstruction
+  OS2_TRY(cudaEventRecord(p->done, p->crt));
+  OS2_TRY(cudaStreamWaitEvent(s, p->done, 0));
+#undef OS2_TRY
+  return OS2_OK;
+}
+
+// run_gemm_panels when A has more than one row panel, else run_gemm.
+os2_status run_gemm_auto(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
+                         int ldb, void *C, int ldc, int N, int mode, void *ws, const Layout &L,
+                         cudaStream_t s) {
+  if (m > 0 && n > 0 && k > 0 && panel_size(m) < m)
+    return run_gemm_panels(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s);
+  return run_gemm(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -385,8 +502,8 @@ os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double 
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
       return OS2_ERR_WORKSPACE;
   }
-  return run_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
-                  static_cast<cudaStream_t>(stream));
+  return run_gemm_auto(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
+                       static_cast<cudaStream_t>(stream));
 }
 
 os2_status os2_sgemm(int m, int n, int k, const float *A, int lda, const float *B, int ldb,
@@ -400,7 +517,7 @@ os2_status os2_sgemm(int m, int n, int k, const float *A, int lda, const float *
     if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
       return OS2_ERR_WORKSPACE;
   }
-  return run_gemm(true, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
+  return run_gemm_auto(true, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, workspace, L,
                   static_cast<cudaStream_t>(stream));
 }
 
@@ -438,7 +555,7 @@ static os2_status complex_gemm(bool f32, int m, int n, int k, const void *A, int
     ProfScope ps("complex_stack", s);
     if ((err = launch_complex_stack(f32, m, n, k, A, lda, B, ldb, A2, B2, s))) return cuda_status(err);
   }
-  st = run_gemm(f32, m, 2 * n, 2 * k, A2, std::max(2 * k, 1), B2, std::max(2 * k, 1), C2,
+  st = run_gemm_auto(f32, m, 2 * n, 2 * k, A2, std::max(2 * k, 1), B2, std::max(2 * k, 1), C2,
                 2 * n, N, mode, ws, L, s);
   if (st) return st;
   ProfScope ps("complex_unstack", s);
@@ -489,20 +606,20 @@ namespace {
 // Host entry point pipeline.  Row panel i of C needs A's row panel i and all
 // of B; a block (row panel, column panel) needs only the two panels.  The
 // operands travel on a copy-in stream in the order A_0, B_0 .. B_{Q-1}, A_1 ..
-// A_{P-1}; the caller's stream scales, splits, multiplies and reconstructs
-// each block as soon as its panels have arrived, while later panels are still
-// in transit; each finished block of C leaves on a copy-out stream while the
-// next block's product runs.  The first and last row panels go block by block
+// A_{P-1}; the caller's stream scales, splits and multiplies each block as
+// soon as its panels have arrived, while later panels are still in transit; a
+// CRT stream reconstructs each block beside the next block's product (see the
+// device-path pipeline), and each finished block of C leaves on a copy-out
+// stream.  The first and last row panels go block by block
 // (a short head before the first product, a short tail after the last); the
 // middle row panels go whole.  Accurate mode's exponents need all of A and all
 // of B, so there the compute waits for every panel; C still leaves by blocks.
-constexpr int kMaxPanels = 8;
-constexpr int kPanelMinRows = 2048;
 
 struct HostPipe {
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, crt = nullptr;
   cudaEvent_t start = nullptr, out_done = nullptr;
-  cudaEvent_t a_in[kMaxPanels] = {}, b_in[kMaxPanels] = {}, c_done[3 * kMaxPanels] = {};
+  cudaEvent_t a_in[kMaxPanels] = {}, b_in[kMaxPanels] = {};
+  cudaEvent_t g_done[3 * kMaxPanels] = {}, c_done[3 * kMaxPanels] = {};
   bool ready = false;
 };
 
@@ -516,7 +633,8 @@ HostPipe *host_pipe() {
   HostPipe &p = pipes[dev];
   if (p.ready) return &p;
   bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess;
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.crt, cudaStreamNonBlocking) == cudaSuccess;
   auto ev = [&](cudaEvent_t *x) {
     ok = ok && cudaEventCreateWithFlags(x, cudaEventDisableTiming) == cudaSuccess;
   };
@@ -526,16 +644,12 @@ HostPipe *host_pipe() {
     ev(&p.a_in[i]);
     ev(&p.b_in[i]);
   }
-  for (int i = 0; i < 3 * kMaxPanels; i++) ev(&p.c_done[i]);
+  for (int i = 0; i < 3 * kMaxPanels; i++) {
+    ev(&p.g_done[i]);
+    ev(&p.c_done[i]);
+  }
   p.ready = ok;
   return ok ? &p : nullptr;
-}
-
-// Panel size along one dimension: at least kPanelMinRows, a multiple of the
-// 256-row tile of step 3, at most kMaxPanels panels.
-int panel_size(int rows) {
-  const int P = std::min(kMaxPanels, std::max(1, rows / kPanelMinRows));
-  return (int)os2_round_up((size_t)((rows + P - 1) / P), 256);
 }
 
 }  // namespace
@@ -650,14 +764,18 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
                              L.ldcres, nullptr, nullptr, 14, t, status, s, n);
       if (err) return cuda_status(err);
     }
+    // the block's CRT runs on the CRT stream beside the next block's product
+    cudaEvent_t gd = p->g_done[blocks], done = p->c_done[blocks];
+    blocks++;
+    if ((err = cudaEventRecord(gd, s))) return cuda_status(err);
+    if ((err = cudaStreamWaitEvent(p->crt, gd, 0))) return cuda_status(err);
     {
-      ProfScope ps("crt_unscale", s);
+      ProfScope ps("crt_unscale", p->crt);
       if ((err = launch_crt(false, mi, nj, ci, L.ldcres, e + r0, f + c0,
-                            dC + (size_t)r0 * n + c0, n, nullptr, t, s)))
+                            dC + (size_t)r0 * n + c0, n, nullptr, t, p->crt)))
         return cuda_status(err);
     }
-    cudaEvent_t done = p->c_done[blocks++];
-    if ((err = cudaEventRecord(done, s))) return cuda_status(err);
+    if ((err = cudaEventRecord(done, p->crt))) return cuda_status(err);
     if ((err = cudaStreamWaitEvent(p->out, done, 0))) return cuda_status(err);
     return cuda_status(copy_rows(C + (size_t)r0 * ldc + c0, ldc, dC + (size_t)r0 * n + c0, n, nj,
                                  mi, cudaMemcpyDeviceToHost, p->out));
@@ -888,7 +1006,10 @@ int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launch
 int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
   if (m <= 0 || n <= 0 || k < 0 || num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return 0;
   if (k == 0) return 0;
-  return mode == OS2_MODE_ACCURATE ? 7 : 4;
+  // os2_gemm: step 1 (fast: 1 kernel; accurate: bars, bound product, two
+  // exponent kernels), then residues, product and CRT once per row panel
+  const int mp = panel_size(m), P = mp < m ? (m + mp - 1) / mp : 1;
+  return (mode == OS2_MODE_ACCURATE ? 4 : 1) + 3 * P;
 }
 
 }  // extern "C"

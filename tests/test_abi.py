@@ -58,6 +58,9 @@ def test_workspace_sizes():
     assert h >= os2.workspace_size(64, 64, 64, 14) + 3 * 64 * 64 * 8
     assert os2.launch_count(64, 64, 64, 14, "fast") == 4
     assert os2.launch_count(64, 64, 64, 14, "accurate") == 7
+    assert os2.launch_count(4095, 64, 64, 14, "fast") == 4          # one row panel
+    assert os2.launch_count(8192, 64, 64, 14, "fast") == 1 + 3 * 4   # four row panels
+    assert os2.launch_count(8192, 64, 64, 14, "accurate") == 4 + 3 * 4
 
 
 def test_argument_errors_are_synchronous():
