@@ -133,8 +133,9 @@ def measured_peaks():
 
 
 def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel's
-    source is unchanged since the capture (else None)."""
+    """DRAM bytes per launch from a committed ncu capture, if the sources that
+    decide the kernel and its launches are unchanged since the capture (else
+    None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -142,12 +143,14 @@ def kernel_traffic(kernel: str):
         d = json.load(fh).get(kernel)
     if not d:
         return None
-    src = os.path.join(ROOT, d["source"])
-    if not os.path.exists(src):
+    if not isinstance(d.get("sources_sha256"), dict) or "bytes_per_launch" not in d:
         return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if h != d["source_sha256"]:
-        return None
+    for rel, want in d["sources_sha256"].items():
+        src = os.path.join(ROOT, rel)
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha256(open(src, "rb").read()).hexdigest() != want:
+            return None
     return d["bytes_per_launch"]
 
 

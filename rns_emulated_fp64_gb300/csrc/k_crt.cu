@@ -7,11 +7,17 @@
 // FP64 rate is low, so instead of the double-double arithmetic the article
 // describes, X is computed exactly in 32-bit integer limbs:
 //   Y_u = sum_l (c_l + 128) W_l,u      unsigned 64-bit sums, no carries yet
-//   Y   = sum_u Y_u 2^(32u) = S + K,   S = sum_l c_l W_l, K = 128 sum_l W_l
-//   q   = nearest integer to (Y - K) / P, estimated in FP32 from the two
-//         highest limb sums (error below 0.003)
-//   X   = Y - K - q P, carries propagated once; if the estimate was within
+//   Y   = sum_u Y_u 2^(32u) = S + 128 sum_l W_l,   S = sum_l c_l W_l
+// The W_l sum to 1 mod P (each is 1 mod its own p_l and 0 mod the others), so
+// Y - 128 = S mod P, and
+//   q   = nearest integer to (Y - 128) / P >= 0, estimated in FP32 from the
+//         two highest limb sums (error below 0.003)
+//   X   = Y - 128 - q P, carries propagated once; if the estimate was within
 //         0.01 of a half-integer, one exact comparison with P/2 fixes q.
+// Only full-rate FP32 and 32-bit integer units are used: the limb sums reach
+// FP32 through 23-bit pieces laid into float bit patterns, and the estimate is
+// rounded by adding 1.5 * 2^23 (64-bit-integer conversions and rounding
+// instructions run on GB300's narrow FP64 and conversion units).
 // X lies in [-P/2, P/2).  [Q] "2の累乗による整数化(手順1と5)": C_ij = X_ij 2^-(e_i+f_j),
 // rounded once to nearest-even from the exact integer (subnormals, overflow).
 //
@@ -160,6 +166,15 @@ __device__ __forceinline__ OutT round_scaled_fast(const uint32_t (&m)[L], bool n
   return ex > F::emax ? F::make(0, 0, neg, 2) : F::make(kept, ex, neg, 0);
 }
 
+// Exact float of x < 2^23 from its bit pattern.
+__device__ __forceinline__ float u23_to_float(uint32_t x) {
+  return __uint_as_float(0x4B000000u | x) - 8388608.0f;
+}
+// fl(y) for y < 2^46, one rounding.
+__device__ __forceinline__ float u46_to_float(uint64_t y) {
+  return fmaf(u23_to_float((uint32_t)(y >> 23)), 8388608.0f, u23_to_float((uint32_t)y & 0x7FFFFFu));
+}
+
 template <int N, typename OutT>
 __global__ void __launch_bounds__(kThreads)
     k_crt(int m, int n, int groups, const int8_t *__restrict__ c, int ldcres,
@@ -204,18 +219,25 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int v = 0; v < LW; v++) Y[v] += (uint64_t)cl * cc.W32[l][v];
     }
-    // q = round((Y - K) / P) from the two top limb sums
-    float t = (float)Y[LW - 1] * cc.s_top - cc.KoverP;
-    if (LW > 1) t = fmaf((float)Y[LW > 1 ? LW - 2 : 0], cc.s_next, t);
-    const float qf = rintf(t);
-    const int q = (int)qf;
-    // X = Y - K - q P in signed 64-bit limb sums, then one carry pass
+    // q = round((Y - 128) / P) from the two top limb sums (each < 2^46)
+    float t = fmaf(u46_to_float(Y[LW - 1]), cc.s_top, -cc.s128);
+    if (LW > 1) t = fmaf(u46_to_float(Y[LW > 1 ? LW - 2 : 0]), cc.s_next, t);
+    const float tq = t + 12582912.0f;  // 1.5 * 2^23: rounds t (-0.5 <= t < 2^13) to an integer
+    int qi = __float_as_int(tq) - 0x4B400000;
+    float qf = tq - 12582912.0f;
+    if (qi < 0) {  // only when Y - 128 is within rounding of -P/2 (then q = 0 is right)
+      qi = 0;
+      qf = 0.0f;
+    }
+    const uint32_t q = (uint32_t)qi;
+    // X = Y - 128 - q P in signed 64-bit limb sums (|each| < 2^46), one carry pass
     uint32_t x[LX];
     long long carry = 0;
 #pragma unroll
     for (int v = 0; v < LX; v++) {
       const long long yv = v < LW ? (long long)Y[v < LW ? v : 0] : 0ll;
-      const long long sv = yv - (long long)cc.K32[v] - (long long)q * (long long)cc.P32[v] + carry;
+      const long long qp = (long long)((uint64_t)q * cc.P32[v]);
+      const long long sv = yv - qp - (v == 0 ? 128 : 0) + carry;
       x[v] = (uint32_t)sv;
       carry = sv >> 32;
     }

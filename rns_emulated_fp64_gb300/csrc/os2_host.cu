@@ -87,16 +87,6 @@ int u_bitlen(const U256 &a) {
     if (a.w[i]) return 32 * i + 32 - __builtin_clz(a.w[i]);
   return 0;
 }
-U256 u_add(const U256 &a, const U256 &b) {
-  U256 r;
-  uint64_t c = 0;
-  for (int i = 0; i < 8; i++) {
-    c += (uint64_t)a.w[i] + b.w[i];
-    r.w[i] = (uint32_t)c;
-    c >>= 32;
-  }
-  return r;
-}
 double u_to_double(const U256 &a) {
   double r = 0;
   for (int i = 7; i >= 0; i--) r = r * 4294967296.0 + (double)a.w[i];
@@ -130,7 +120,6 @@ void build_tables(int N, Os2Tables *t) {
   const U256 H = u_shr1(u_sub1(P));  // floor((P-1)/2)
   const U256 half = u_shr1(P);       // P/2 (P is even: 256 is a modulus)
   t->res.N = t->crt.N = t->gemm.N = N;
-  U256 Ksum = u_from(0);
   for (int l = 0; l < N; l++) {
     const int p = kModuli[l];
     t->p[l] = p;
@@ -150,21 +139,16 @@ void build_tables(int N, Os2Tables *t) {
       pw = (int)(((long long)pw * 4096) % p);
     }
     for (int v = 0; v < 5; v++) t->crt.W32[l][v] = W.w[v];
-    Ksum = u_add(Ksum, W);
   }
-  const U256 K = u_mul(Ksum, 128);
   for (int v = 0; v < 6; v++) {
     t->crt.P32[v] = P.w[v];
-    t->crt.K32[v] = K.w[v];
     t->crt.H32[v] = half.w[v];
   }
   const int LW = (N + 3) / 4;
   const double Pd = u_to_double(P);
   t->crt.s_top = (float)(ldexp(1.0, 32 * (LW - 1)) / Pd);
   t->crt.s_next = (float)(LW > 1 ? ldexp(1.0, 32 * (LW - 2)) / Pd : 0.0);
-  double kop = 0;
-  for (int l = 0; l < N; l++) kop += 128.0 * t->inv[l] / (double)kModuli[l];
-  t->crt.KoverP = (float)kop;
+  t->crt.s128 = (float)(128.0 / Pd);
   for (int i = 0; i < OS2_H_LIMBS; i++) t->res.H[i] = H.w[i];
   t->res.bitlenH = u_bitlen(H);
 }

@@ -29,10 +29,9 @@ struct CrtConsts {
   int N;
   uint32_t W32[OS2_MAX_MODULI][5];   // W_l = M_l inv_l
   uint32_t P32[6];                   // P
-  uint32_t K32[6];                   // K = 128 sum_l W_l (offset of the unsigned residues)
   uint32_t H32[6];                   // P / 2
   float s_top, s_next;               // fl(2^(32(LW-1)) / P), fl(2^(32(LW-2)) / P), LW = (N+3)/4
-  float KoverP;                      // fl(K / P)
+  float s128;                        // fl(128 / P)
 };
 
 // Step-3 constants.

@@ -190,6 +190,28 @@ def test_crt_parity_from_oracle_residues(N):
     assert_bits_equal(C.cpu().numpy(), ref.C, "C")
 
 
+@pytest.mark.parametrize("N", [1, 2])
+def test_crt_exhaustive_small_moduli_sets(N):
+    """Every residue vector for N = 1 (256 values) and N = 2 (256 x 255):
+    X is the unique value in [-P/2, P/2) with those residues (brute force),
+    including X = -P/2 itself; with e = f = 0 the result is X exactly."""
+    mods = os2.moduli(N)
+    P = int(np.prod(mods))
+    grids = np.meshgrid(*[np.arange(-(p // 2), (p + 1) // 2) for p in mods], indexing="ij")
+    res = np.stack([g.reshape(-1) for g in grids])          # N x P residue vectors
+    vals = np.arange(-P // 2, P // 2)                          # brute force: residues of each X
+    sym = np.stack([((vals + p // 2) % p) - p // 2 for p in mods])
+    lookup = {tuple(col): int(x) for col, x in zip(sym.T, vals)}
+    expect = np.array([lookup[tuple(col)] for col in res.T], dtype=np.float64)
+    n = 256
+    m = P // n
+    cres = np.zeros((N, m, n), np.int8)
+    cres[:, :, :] = res.reshape(N, m, n)
+    C = os2.crt(dev(cres), n, dev(np.zeros(m, np.int32)), dev(np.zeros(n, np.int32)))
+    status_ok()
+    assert np.array_equal(C.cpu().numpy().reshape(-1), expect)
+
+
 def test_crt_random_residues_and_rounding():
     """Arbitrary residue vectors (X anywhere in [-P/2, P/2)) and exponents that
     push the result into the subnormal and overflow ranges."""
