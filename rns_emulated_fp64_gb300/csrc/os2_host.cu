@@ -600,9 +600,10 @@ namespace {
 // of B, so there the compute waits for every panel; C still leaves by blocks.
 
 struct HostPipe {
-  cudaStream_t in = nullptr, out = nullptr, crt = nullptr;
+  cudaStream_t in = nullptr, out = nullptr, crt = nullptr, res = nullptr;
   cudaEvent_t start = nullptr, out_done = nullptr;
   cudaEvent_t a_in[kMaxPanels] = {}, b_in[kMaxPanels] = {};
+  cudaEvent_t a_split[kMaxPanels] = {}, b_split[kMaxPanels] = {};
   cudaEvent_t g_done[3 * kMaxPanels] = {}, c_done[3 * kMaxPanels] = {};
   bool ready = false;
 };
@@ -618,7 +619,8 @@ HostPipe *host_pipe() {
   if (p.ready) return &p;
   bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
             cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess &&
-            cudaStreamCreateWithFlags(&p.crt, cudaStreamNonBlocking) == cudaSuccess;
+            cudaStreamCreateWithFlags(&p.crt, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.res, cudaStreamNonBlocking) == cudaSuccess;
   auto ev = [&](cudaEvent_t *x) {
     ok = ok && cudaEventCreateWithFlags(x, cudaEventDisableTiming) == cudaSuccess;
   };
@@ -627,6 +629,8 @@ HostPipe *host_pipe() {
   for (int i = 0; i < kMaxPanels; i++) {
     ev(&p.a_in[i]);
     ev(&p.b_in[i]);
+    ev(&p.a_split[i]);
+    ev(&p.b_split[i]);
   }
   for (int i = 0; i < 3 * kMaxPanels; i++) {
     ev(&p.g_done[i]);
@@ -698,43 +702,61 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
   }
   for (int i = 1; i < P; i++) OS2_TRY(send_a(i));
 
-  // steps 1 + 2 for row panel i of A (fast mode: the panel's exponents too);
-  // the panel's planes are laid out as an mi-row problem
+  // Steps 1 + 2 of each panel ("splits").  Fast mode: on a split stream, each
+  // as soon as its panel has arrived, so that a panel is scaled and split
+  // while the previous block is multiplied.  Accurate mode: on `stream`, after
+  // the exponents (which need all of A and B).
+  const bool side = mode == OS2_MODE_FAST;
+  cudaStream_t sp = side ? p->res : s;
+  // row panel i of A (the panel's planes are laid out as an mi-row problem)
   auto split_a = [&](int i) {
     const int r0 = i * mp, mi = std::min(mp, m - r0);
     const double *Ai = dA + (size_t)r0 * k;
     cudaError_t r = cudaSuccess;
-    if (mode == OS2_MODE_FAST) {
-      if ((r = cudaStreamWaitEvent(s, p->a_in[i], 0))) return r;
-      ProfScope ps("scale", s);
+    if (side) {
+      if ((r = cudaStreamWaitEvent(sp, p->a_in[i], 0))) return r;
+      ProfScope ps("scale", sp);
       r = launch_row_scale(SM_FAST_SCALE, false, Ai, k, mi, e + r0, nullptr, nullptr, nullptr, 0,
-                           0, nullptr, nullptr, nullptr, k, L.kp, t, status, s);
+                           0, nullptr, nullptr, nullptr, k, L.kp, t, status, sp);
       if (r) return r;
     }
-    ProfScope ps("residues", s);
-    return launch_residues(false, Ai, k, mi, e + r0, pa + (size_t)r0 * N * plane_row, nullptr, 0,
-                           0, nullptr, nullptr, k, L.kp, t, s);
+    {
+      ProfScope ps("residues", sp);
+      r = launch_residues(false, Ai, k, mi, e + r0, pa + (size_t)r0 * N * plane_row, nullptr, 0,
+                          0, nullptr, nullptr, k, L.kp, t, sp);
+    }
+    return r ? r : (side ? cudaEventRecord(p->a_split[i], sp) : cudaSuccess);
   };
-  // steps 1 + 2 for column panel j of B, in place in B's [N][n][kp] planes
+  // column panel j of B, in place in B's [N][n][kp] planes
   auto split_b = [&](int j) {
     const int c0 = j * nq, nj = std::min(nq, n - c0);
     const double *Bj = dB + (size_t)c0 * k;
     cudaError_t r = cudaSuccess;
-    if (mode == OS2_MODE_FAST) {
-      if ((r = cudaStreamWaitEvent(s, p->b_in[j], 0))) return r;
-      ProfScope ps("scale", s);
+    if (side) {
+      if ((r = cudaStreamWaitEvent(sp, p->b_in[j], 0))) return r;
+      ProfScope ps("scale", sp);
       r = launch_row_scale(SM_FAST_SCALE, false, nullptr, 0, 0, nullptr, nullptr, nullptr, Bj, k,
-                           nj, f + c0, nullptr, nullptr, k, L.kp, t, status, s);
+                           nj, f + c0, nullptr, nullptr, k, L.kp, t, status, sp);
       if (r) return r;
     }
-    ProfScope ps("residues", s);
-    return launch_residues(false, nullptr, 0, 0, nullptr, nullptr, Bj, k, nj, f + c0,
-                           pb + (size_t)c0 * plane_row, k, L.kp, t, s, n);
+    {
+      ProfScope ps("residues", sp);
+      r = launch_residues(false, nullptr, 0, 0, nullptr, nullptr, Bj, k, nj, f + c0,
+                          pb + (size_t)c0 * plane_row, k, L.kp, t, sp, n);
+    }
+    return r ? r : (side ? cudaEventRecord(p->b_split[j], sp) : cudaSuccess);
   };
-  // steps 3-5 for the block (row panel i, columns c0 .. c0+nj), then its copy out
+  // steps 3-5 for the block (row panel i, columns c0 .. c0+nj of column
+  // panel j, or all columns when j < 0), then its copy out
   int blocks = 0;
-  auto block = [&](int i, int c0, int nj) -> os2_status {
+  auto block = [&](int i, int j, int c0, int nj) -> os2_status {
     const int r0 = i * mp, mi = std::min(mp, m - r0);
+    if (side) {
+      // the split stream runs in arrival order: A_0, B_0 .. B_{Q-1}, A_1 ..
+      if ((err = cudaStreamWaitEvent(s, p->a_split[i], 0))) return cuda_status(err);
+      if (i == 0 && j >= 0 && (err = cudaStreamWaitEvent(s, p->b_split[j], 0)))
+        return cuda_status(err);
+    }
     const void *pai = pa + (size_t)r0 * N * plane_row;
     int8_t *ci = cres + (size_t)r0 * N * L.ldcres + c0;
     const char *pbj = pb + (size_t)c0 * plane_row;
@@ -765,11 +787,10 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
                                  mi, cudaMemcpyDeviceToHost, p->out));
   };
   auto row_panel = [&](int i, bool by_blocks) -> os2_status {
-    if (!by_blocks) return block(i, 0, n);
+    if (!by_blocks) return block(i, -1, 0, n);
     for (int j = 0; j < Q; j++) {
       const int c0 = j * nq;
-      if (i == 0) OS2_TRY(split_b(j));
-      if ((st = block(i, c0, std::min(nq, n - c0)))) return st;
+      if ((st = block(i, j, c0, std::min(nq, n - c0)))) return st;
     }
     return OS2_OK;
   };
@@ -781,11 +802,10 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
       return st;
   }
   OS2_TRY(split_a(0));
-  if ((st = row_panel(0, true))) return st;
-  for (int i = 1; i < P; i++) {
-    OS2_TRY(split_a(i));
-    if ((st = row_panel(i, i == P - 1))) return st;
-  }
+  for (int j = 0; j < Q; j++) OS2_TRY(split_b(j));
+  for (int i = 1; i < P; i++) OS2_TRY(split_a(i));
+  for (int i = 0; i < P; i++)
+    if ((st = row_panel(i, i == 0 || i == P - 1))) return st;
   // `stream` covers everything: it waits for the last copy out
   OS2_TRY(cudaEventRecord(p->out_done, p->out));
   OS2_TRY(cudaStreamWaitEvent(s, p->out_done, 0));
