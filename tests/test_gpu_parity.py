@@ -549,3 +549,54 @@ def test_zgemm_integer_inputs_exact_on_gpu():
     C = os2.zgemm(dev(Z.astype(np.complex128)), dev(W.astype(np.complex128)), 14).cpu().numpy()
     status_ok()
     assert np.array_equal(C, Z @ W.T)
+
+
+# ------------------------------------------------------- row-panel pipeline --
+def test_row_panels_equal_unpanelled_rows():
+    """m >= 4096 runs A in row panels with the CRT on a side stream.  Fast-mode
+    exponents depend on one row or one column only, so the panelled product
+    equals, entry for entry, two calls on halves of A (each a single panel)."""
+    A, Bt = workloads.make_pair("spread", 4100, 520, 300, seed=21, phi=1.5)
+    C = os2.gemm(dev(A), dev(Bt), 16, "fast").cpu().numpy()
+    status_ok()
+    top = os2.gemm(dev(A[:2050]), dev(Bt), 16, "fast").cpu().numpy()
+    bot = os2.gemm(dev(A[2050:]), dev(Bt), 16, "fast").cpu().numpy()
+    status_ok()
+    assert_bits_equal(C, np.vstack([top, bot]), "panelled vs halves")
+
+
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+@pytest.mark.parametrize("m", [4100, 9000])
+def test_row_panels_oracle_sample(mode, m):
+    """Ragged last panel (4100 = 2304 + 1796; 9000 = 3 x 2304 + 2088), both
+    modes, a seeded 40 x 40 sample (always with the last row and column)
+    bit-exact against the oracle."""
+    n, k = 200, 160
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=m, phi=2.0)
+    C = os2.gemm(dev(A), dev(Bt), 14, mode).cpu().numpy()
+    status_ok()
+    rows, cols = workloads.sample_grid(m, n, 40, seed=3)
+    ref = orc.gemm_entries(A, Bt, 14, rows, cols, mode=orc.FAST if mode == "fast" else orc.ACCURATE,
+                           want_X=False, want_c=False, want_G=False)
+    assert ref.mismatches == 0
+    assert_bits_equal(C[np.ix_(rows, cols)], ref.C, f"panels m={m} {mode}")
+
+
+def test_row_panels_sgemm_and_zgemm_sample():
+    """SGEMM and ZGEMM emulation also take the row-panel path for m >= 4096."""
+    m, n, k = 4100, 96, 130
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=5, phi=1.0)
+    A32, B32 = A.astype(np.float32), Bt.astype(np.float32)
+    C = os2.sgemm(dev(A32), dev(B32), 7, "fast").cpu().numpy()
+    status_ok()
+    rows, cols = workloads.sample_grid(m, n, 32, seed=4)
+    ref = orc.gemm_entries(A32, B32, 7, rows, cols, want_X=False, want_c=False, want_G=False,
+                           out_f32=True)
+    _f32_bits_equal(C[np.ix_(rows, cols)], ref.C, "sgemm panels")
+    Ai, Bi = workloads.make_pair("spread", m, n, k, seed=6, phi=1.0)
+    Z, W = A + 1j * Ai, Bt + 1j * Bi
+    Cz = os2.zgemm(dev(Z), dev(W), 16, "fast").cpu().numpy()
+    status_ok()
+    refz, r = orc.complex_gemm_entries(Z, W, 16, rows, cols)
+    assert r.mismatches == 0
+    assert np.array_equal(Cz[np.ix_(rows, cols)].view(np.uint64), refz.view(np.uint64))
