@@ -406,10 +406,89 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kStages2 = 6;
 constexpr int kHalf = 128;
 
+// Accurate-mode bound product on the 2-SM kernel (BOUND = 1): one launch per
+// segment of at most 64 k-blocks, whose FP32 sums (Abar, Bbar <= 64, so each
+// product <= 2^12 and a segment's sum <= 2^24) are exact.  Segments after the
+// first add the int32 partial sums of the earlier ones; the last takes the
+// row and column maxima.
+struct BoundSeg {
+  int kb_begin;          // first k-block of the segment
+  int first, last;       // segment flags
+  int32_t *partial;      // int32 [m][ldp] partial sums between segments
+  int ldp;
+  int32_t *rowmax, *colmax;
+};
+
+// Bound-segment epilogue: this thread's row `grow` of the tile, 256 columns
+// from col0, read from TMEM as exact FP32 integers.  Rows and columns past the
+// matrix hold 0 (zero-filled operand tiles), which never changes a maximum.
+// The partial sums move as 16-byte vectors (ldp is a multiple of 4), and a
+// group's partial loads are issued before its TMEM load is waited on.
+__device__ __forceinline__ void bound_epilogue(uint32_t taddr, int grow, int col0, int lane,
+                                               const Sched &sp, const BoundSeg &bs) {
+  const bool row_ok = grow < sp.m;
+  int rmax = 0;
+#pragma unroll 1
+  for (int g = 0; g < 256 / 32; g++) {
+    const int cb = col0 + g * 32;
+    const bool full = cb + 32 <= sp.n;
+    int4 *prow = reinterpret_cast<int4 *>(bs.partial + (size_t)(row_ok ? grow : 0) * bs.ldp + cb);
+    int4 pv[8];
+    if (!bs.first && row_ok && full) {
+#pragma unroll
+      for (int q = 0; q < 8; q++) pv[q] = prow[q];
+    }
+    uint32_t v[32];
+    tmem_ld32(taddr + g * 32, v);
+    tmem_wait_ld();
+    int x[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) x[i] = __float2int_rn(__uint_as_float(v[i]));
+    int *ps = reinterpret_cast<int *>(prow);
+    if (!bs.first && row_ok) {
+      if (full) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+          x[4 * q] += pv[q].x;
+          x[4 * q + 1] += pv[q].y;
+          x[4 * q + 2] += pv[q].z;
+          x[4 * q + 3] += pv[q].w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++)
+          if (cb + i < sp.n) x[i] += ps[i];
+      }
+    }
+    if (!bs.last) {
+      if (row_ok) {
+        if (full) {
+#pragma unroll
+          for (int q = 0; q < 8; q++)
+            prow[q] = make_int4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i++)
+            if (cb + i < sp.n) ps[i] = x[i];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        rmax = max(rmax, x[i]);
+        const int cm = __reduce_max_sync(0xffffffffu, x[i]);  // over the warp's 32 rows
+        if (lane == i && cb + i < sp.n) atomicMax(&bs.colmax[cb + i], cm);
+      }
+    }
+  }
+  if (bs.last && row_ok) atomicMax(&bs.rowmax[grow], rmax);
+}
+
+template <int BOUND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                const Sched sp, const GemmConsts gc, int8_t *__restrict__ out, int ldo,
-               int *status) {
+               const BoundSeg bs, int *status) {
   constexpr int BN = 256, STAGES = kStages2;
   constexpr uint32_t A_BYTES = kHalf * BK * 2, B_BYTES = kHalf * BK * 2;
   constexpr uint32_t IDESC = idesc_f16_f32(2 * kHalf, BN);
@@ -476,9 +555,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
-          tma_load_3d_pair(sA + stage * A_BYTES, &mapA, fbar, kb * BK,
+          const int kx = (BOUND ? bs.kb_begin + kb : kb) * BK;
+          tma_load_3d_pair(sA + stage * A_BYTES, &mapA, fbar, kx,
                            tm * 2 * kHalf + (int)rank * kHalf, l);
-          tma_load_3d_pair(sB + stage * B_BYTES, &mapB, fbar, kb * BK,
+          tma_load_3d_pair(sB + stage * B_BYTES, &mapB, fbar, kx,
                            tn * BN + (int)rank * kHalf, l);
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -561,7 +641,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       job_coords(job, sp, l, tm, tn);
       const float p = gc.p[l], invp = gc.invp[l];
       const uint32_t taddr = lane_base + (uint32_t)(buf * BN);
-      if (c != sp.nchunks - 1) {
+      if (BOUND) {
+        bound_epilogue(taddr, tm * 2 * kHalf + (int)rank * kHalf + r_in_tile, tn * BN, lane, sp,
+                       bs);
+      } else if (c != sp.nchunks - 1) {
 #pragma unroll 1
         for (int g = 0; g < BN / 32; g++) {
           uint32_t v[32];
@@ -701,36 +784,81 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
   return cudaGetLastError();
 }
 
-cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
-                    int ldo, const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows) {
+template <int BOUND>
+cudaError_t set_smem2() {
   constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem);
+    attr_err = cudaFuncSetAttribute(k_gemm_tc2<BOUND>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
+  return attr_err;
+}
+
+Sched sched2(int m, int n, int kb_total, int nplanes) {
+  Sched sp;
+  sp.m = m;
+  sp.n = n;
+  sp.kb_total = kb_total;
+  sp.tiles_m = (m + 2 * kHalf - 1) / (2 * kHalf);
+  sp.tiles_n = (n + 255) / 256;
+  sp.tiles = sp.tiles_m * sp.tiles_n;
+  sp.njobs = sp.tiles * nplanes;
+  return sp;
+}
+
+cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
+                    int ldo, const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows) {
+  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
+  cudaError_t attr_err = set_smem2<0>();
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
   if (!make_map(&ma, RA, kp, m, nplanes, kHalf, m) ||
       !make_map(&mb, RB, kp, n, nplanes, kHalf, b_plane_rows))
     return cudaErrorInvalidValue;
-  Sched sp;
-  sp.m = m;
-  sp.n = n;
-  sp.kb_total = kp / BK;
-  sp.tiles_m = (m + 2 * kHalf - 1) / (2 * kHalf);
-  sp.tiles_n = (n + 255) / 256;
-  sp.tiles = sp.tiles_m * sp.tiles_n;
-  sp.njobs = sp.tiles * nplanes;
+  Sched sp = sched2(m, n, kp / BK, nplanes);
   sp.chunk = (int)(((1LL << 24) - 135) / ((long long)BK << 14));
   sp.nchunks = (sp.kb_total + sp.chunk - 1) / sp.chunk;
   if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
   const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
   GemmConsts gc = t ? t->gemm : GemmConsts{};
-  k_gemm_tc2<<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, gc, reinterpret_cast<int8_t *>(out), ldo,
-                                               status);
+  k_gemm_tc2<0><<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, gc, reinterpret_cast<int8_t *>(out),
+                                                  ldo, BoundSeg{}, status);
   return cudaGetLastError();
+}
+
+// Accurate-mode bound product (magnitude planes <= 64) with fused row and
+// column maxima on the 2-SM kernel, in segments of at most 64 k-blocks.
+cudaError_t launch2_bound(int m, int n, int kp, const void *RA, const void *RB, int32_t *partial,
+                          int ldp, int32_t *rowmax, int32_t *colmax, int *status,
+                          cudaStream_t s) {
+  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
+  constexpr int kSegMax = (int)((1LL << 24) / ((long long)BK << 12));  // 64 k-blocks
+  cudaError_t attr_err = set_smem2<1>();
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, RA, kp, m, 1, kHalf, m) || !make_map(&mb, RB, kp, n, 1, kHalf, n))
+    return cudaErrorInvalidValue;
+  const int kb_all = kp / BK;
+  const int segs = (kb_all + kSegMax - 1) / kSegMax;
+  if (segs > 1 && (!partial || ldp < n || ldp % 4 != 0 ||
+                   (reinterpret_cast<uintptr_t>(partial) & 15)))
+    return cudaErrorInvalidValue;
+  for (int g = 0; g < segs; g++) {
+    const int kb0 = (int)((long long)g * kb_all / segs), kb1 = (int)((long long)(g + 1) * kb_all / segs);
+    Sched sp = sched2(m, n, kb1 - kb0, 1);
+    sp.chunk = sp.kb_total;
+    sp.nchunks = 1;
+    if (sp.njobs == 0 || sp.kb_total == 0) return cudaSuccess;
+    const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
+    const BoundSeg bs{kb0, g == 0, g == segs - 1, partial, ldp, rowmax, colmax};
+    k_gemm_tc2<1><<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, GemmConsts{}, nullptr, 0, bs,
+                                                    status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -748,4 +876,11 @@ cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const
                      status, s, b_plane_rows);
   return launch<1>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
                    status, s, b_plane_rows);
+}
+
+cudaError_t launch_gemm_bound2(int m, int n, int kp, const void *RA, const void *RB,
+                               int32_t *partial, int ldp, int32_t *rowmax, int32_t *colmax,
+                               int *status, cudaStream_t s) {
+  if (m <= 0 || n <= 0 || kp <= 0) return cudaSuccess;
+  return launch2_bound(m, n, kp, RA, RB, partial, ldp, rowmax, colmax, status, s);
 }

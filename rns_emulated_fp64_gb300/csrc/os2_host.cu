@@ -266,6 +266,22 @@ os2_status check_gemm_args(int m, int n, int k, const void *A, int lda, const vo
   return OS2_OK;
 }
 
+// The exact bound product of accurate mode with fused row/column maxima into
+// R, K (zeroed): on the 2-SM kernel when it is the selected step-3 kernel and
+// either k fits one 4096-term segment or the product-residue region of the
+// workspace (unused during step 1) can hold the int32 partial sums; else on
+// the single-SM kernel, which sums its segments in registers.
+cudaError_t bound_product(int m, int n, const Layout &L, void *ws, const void *pa, const void *pb,
+                          int32_t *R, int32_t *K, const Os2Tables *t, int *status,
+                          cudaStream_t s) {
+  const int segs = (L.kp + 4095) / 4096;
+  const bool room = L.total - L.cres >= 4 * (size_t)m * (size_t)L.ldcres;
+  if (g_variant.load() == OS2_GEMM_TC && (segs == 1 || room))
+    return launch_gemm_bound2(m, n, L.kp, pa, pb, at<int32_t>(ws, L.cres), L.ldcres, R, K, status,
+                              s);
+  return launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s);
+}
+
 // Step 1 in accurate mode: magnitude planes (aliasing the residue planes), one
 // exact bound product with fused row/column maxima, then the exponents e, f.
 os2_status accurate_exponents(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
@@ -286,8 +302,7 @@ os2_status accurate_exponents(bool f32, int m, int n, int k, const void *A, int 
   if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
   {
     ProfScope ps("gemm_bound", s);
-    if ((err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
-      return cuda_status(err);
+    if ((err = bound_product(m, n, L, ws, pa, pb, R, K, t, status, s))) return cuda_status(err);
   }
   if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
   return cuda_status(launch_accu_exponents(K, EB, n, f, t, s));
@@ -847,8 +862,7 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
     return cuda_status(err);
   if ((err = cudaMemsetAsync(R, 0, 4 * (size_t)std::max(m, 1), s))) return cuda_status(err);
   if ((err = cudaMemsetAsync(K, 0, 4 * (size_t)std::max(n, 1), s))) return cuda_status(err);
-  if (m > 0 && n > 0 &&
-      (err = launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s)))
+  if (m > 0 && n > 0 && (err = bound_product(m, n, L, workspace, pa, pb, R, K, t, status, s)))
     return cuda_status(err);
   if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
   return cuda_status(launch_accu_exponents(K, EB, n, f, t, s));

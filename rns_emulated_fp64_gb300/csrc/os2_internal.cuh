@@ -95,6 +95,16 @@ cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const
                            int prod_bound_log2, const Os2Tables *t, int *status, cudaStream_t s,
                            int b_plane_rows = 0);
 
+// Accurate-mode bound product with fused row/column maxima on the 2-SM
+// kernel: magnitude planes (one FP16 plane each, values <= 64) of A (m rows)
+// and B (n rows); atomicMax into rowmax[m] and colmax[n] (zeroed by the
+// caller).  k is taken in segments of 4096 (64 k-blocks); with more than one
+// segment, partial (int32 [m][ldp], ldp >= n a multiple of 4, 16-byte
+// aligned) holds the sums between them.
+cudaError_t launch_gemm_bound2(int m, int n, int kp, const void *RA, const void *RB,
+                               int32_t *partial, int ldp, int32_t *rowmax, int32_t *colmax,
+                               int *status, cudaStream_t s);
+
 // Complex products: interleaved complex operands <-> stacked real operands.
 cudaError_t launch_complex_stack(bool f32, int m, int n, int k, const void *A, long lda,
                                  const void *B, long ldb, void *A2, void *Bt2, cudaStream_t s);
