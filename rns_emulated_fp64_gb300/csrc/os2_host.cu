@@ -271,12 +271,21 @@ os2_status check_gemm_args(int m, int n, int k, const void *A, int lda, const vo
 // either k fits one 4096-term segment or the product-residue region of the
 // workspace (unused during step 1) can hold the int32 partial sums; else on
 // the single-SM kernel, which sums its segments in registers.
+bool bound_on_2sm(int m, const Layout &L) {
+  const int segs = (L.kp + 4095) / 4096;
+  const bool room = L.total - L.cres >= 4 * (size_t)m * (size_t)L.ldcres;
+  return g_variant.load() == OS2_GEMM_TC && (segs == 1 || room);
+}
+
+// Kernel launches of bound_product.
+int bound_launches(int m, int, const Layout &L) {
+  return bound_on_2sm(m, L) ? (L.kp + 4095) / 4096 : 1;
+}
+
 cudaError_t bound_product(int m, int n, const Layout &L, void *ws, const void *pa, const void *pb,
                           int32_t *R, int32_t *K, const Os2Tables *t, int *status,
                           cudaStream_t s) {
-  const int segs = (L.kp + 4095) / 4096;
-  const bool room = L.total - L.cres >= 4 * (size_t)m * (size_t)L.ldcres;
-  if (g_variant.load() == OS2_GEMM_TC && (segs == 1 || room))
+  if (bound_on_2sm(m, L))
     return launch_gemm_bound2(m, n, L.kp, pa, pb, at<int32_t>(ws, L.cres), L.ldcres, R, K, status,
                               s);
   return launch_gemm_tc(1, m, n, L.kp, pa, pb, 1, nullptr, 0, R, K, 12, t, status, s);
@@ -1024,10 +1033,13 @@ int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launch
 int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
   if (m <= 0 || n <= 0 || k < 0 || num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return 0;
   if (k == 0) return 0;
-  // os2_gemm: step 1 (fast: 1 kernel; accurate: bars, bound product, two
-  // exponent kernels), then residues, product and CRT once per row panel
+  // os2_gemm: step 1 (fast: 1 kernel; accurate: bars, the bound product,
+  // two exponent kernels), then residues, product and CRT once per row panel
   const int mp = panel_size(m), P = mp < m ? (m + mp - 1) / mp : 1;
-  return (mode == OS2_MODE_ACCURATE ? 4 : 1) + 3 * P;
+  if (mode != OS2_MODE_ACCURATE) return 1 + 3 * P;
+  Layout L;
+  if (!make_layout(m, n, k, num_moduli, mode, &L)) return 0;
+  return 3 + bound_launches(m, n, L) + 3 * P;
 }
 
 }  // extern "C"

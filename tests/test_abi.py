@@ -61,6 +61,7 @@ def test_workspace_sizes():
     assert os2.launch_count(4095, 64, 64, 14, "fast") == 4          # one row panel
     assert os2.launch_count(8192, 64, 64, 14, "fast") == 1 + 3 * 4   # four row panels
     assert os2.launch_count(8192, 64, 64, 14, "accurate") == 4 + 3 * 4
+    assert os2.launch_count(8192, 64, 8192, 14, "accurate") == 3 + 2 + 3 * 4   # 2 bound segments
 
 
 def test_argument_errors_are_synchronous():
