@@ -9,8 +9,10 @@
 // magnitude, so the k loop is cut into chunks and the accumulator is reduced
 // between chunks ("lazy" reduction: only when it could otherwise overflow):
 //
-//  KIND 0 (mod-p output): 128x256 tiles.  After each chunk of 15 k-blocks
-//    (960 terms, |partial| <= 134 + 960 * 2^14 < 2^24) the epilogue warps read
+//  KIND 0 (mod-p output): 128x256 tiles.  The k loop is cut into
+//    ceil(k-blocks / 15) chunks of at most 15 k-blocks, with lengths that
+//    differ by at most one.  After each chunk (at most 960 terms, |partial| <=
+//    134 + 960 * 2^14 < 2^24) the epilogue warps read
 //    the accumulator, subtract the nearest multiple of p_l and write the small
 //    remainder back; the next chunk accumulates on top of it.  Two jobs (tile x
 //    modulus) are interleaved chunk by chunk, one per TMEM buffer, so the MMA
@@ -21,7 +23,11 @@
 //    accumulator (ping-pong between two TMEM buffers); the epilogue converts it
 //    to int32 and adds it to a running sum held in registers.  Outputs: the raw
 //    int32 product (parity checks) and/or its row and column maxima (the bound
-//    product of the accurate mode).
+//    product of the accurate mode, where the 2-SM kernel below cannot be used).
+//
+//  k_gemm_tc2 (further down): the same mod-p product on CTA pairs with 256x256
+//    tiles (the default), and the accurate-mode bound product in 4096-term
+//    segments.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over jobs):
 //   warp 0     TMA producer: 128-byte-swizzled k-blocks of A and B into a
