@@ -602,23 +602,24 @@ def test_row_panels_sgemm_and_zgemm_sample():
     assert np.array_equal(Cz[np.ix_(rows, cols)].view(np.uint64), refz.view(np.uint64))
 
 
-@pytest.mark.parametrize("k", [4096, 4097, 9000])
-def test_accurate_bound_segments(k):
+@pytest.mark.parametrize("N,k", [(16, 4096), (16, 4097), (16, 9000), (2, 9000)])
+def test_accurate_bound_segments(N, k):
     """Accurate mode's bound product runs in 4096-term segments on the 2-SM
     kernel (int32 partial sums between segments, ragged n); os2_scale, whose
     own workspace has no room for the partial sums, takes the single-SM kernel
     for more than one segment.  Both give the oracle's exponents, and the
-    product is bit-exact."""
+    product is bit-exact.  With N = 2 the product-residue region is too small
+    for the partial sums, so os2_gemm falls back to the single-SM kernel too."""
     m, n = 300, 70
     A, Bt = workloads.make_pair("spread", m, n, k, seed=k, phi=2.0)
-    e_ref, f_ref = orc.scale_accu(A, Bt, 16)
-    e, f = os2.scale(dev(A), dev(Bt), 16, "accurate")
+    e_ref, f_ref = orc.scale_accu(A, Bt, N)
+    e, f = os2.scale(dev(A), dev(Bt), N, "accurate")
     status_ok()
     assert np.array_equal(e.cpu().numpy(), e_ref)
     assert np.array_equal(f.cpu().numpy(), f_ref)
-    C = os2.gemm(dev(A), dev(Bt), 16, "accurate").cpu().numpy()
+    C = os2.gemm(dev(A), dev(Bt), N, "accurate").cpu().numpy()
     status_ok()
     rows, cols = workloads.sample_grid(m, n, 24, seed=2)
-    ref = orc.gemm_entries(A, Bt, 16, rows, cols, mode=orc.ACCURATE, want_X=False, want_c=False,
+    ref = orc.gemm_entries(A, Bt, N, rows, cols, mode=orc.ACCURATE, want_X=False, want_c=False,
                            want_G=False)
     assert_bits_equal(C[np.ix_(rows, cols)], ref.C, f"accurate k={k}")
