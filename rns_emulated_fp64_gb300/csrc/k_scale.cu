@@ -192,17 +192,25 @@ __global__ void __launch_bounds__(kThreads)
   // pass 1: exponent bound and finiteness
   int emax = INT_MIN, bad = 0;
   if (vec) {
-    for (int h = 2 * threadIdx.x; h < k; h += 2 * kThreads) {
-      if (h + 1 < k) {
-        T v0, v1;
-        load2(x + h, v0, v1);
-        const Dec d0 = decode(v0), d1 = decode(v1);
-        bad |= d0.nonfinite | d1.nonfinite;
-        emax = max(emax, max(exp_bound(d0), exp_bound(d1)));
-      } else {
-        const Dec d0 = decode(__ldg(x + h));
-        bad |= d0.nonfinite;
-        emax = max(emax, exp_bound(d0));
+    // four independent 2-entry loads per thread in flight before any is used
+    constexpr int U = 4;
+    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kThreads * U) {
+      T v[2 * U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int h = h0 + u * 2 * kThreads;
+        if (h + 1 < k) {
+          load2(x + h, v[2 * u], v[2 * u + 1]);
+        } else {
+          v[2 * u] = h < k ? __ldg(x + h) : T(0);
+          v[2 * u + 1] = T(0);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 2 * U; i++) {
+        const Dec d = decode(v[i]);
+        bad |= d.nonfinite;
+        emax = max(emax, exp_bound(d));
       }
     }
   } else {
@@ -240,10 +248,33 @@ __global__ void __launch_bounds__(kThreads)
   // (each q^2 <= 2^46; a thread's partial stays below 2^64 for k < 2^26;
   // the block sum is 128-bit)
   unsigned long long Q = 0, Qhi = 0;
-  for (int h = threadIdx.x; h < k; h += kThreads) {
-    const Dec d = decode(__ldg(x + h));
-    const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
-    Q += q * q;
+  if (vec) {
+    constexpr int U = 4;
+    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kThreads * U) {
+      T v[2 * U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int h = h0 + u * 2 * kThreads;
+        if (h + 1 < k) {
+          load2(x + h, v[2 * u], v[2 * u + 1]);
+        } else {
+          v[2 * u] = h < k ? __ldg(x + h) : T(0);
+          v[2 * u + 1] = T(0);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 2 * U; i++) {
+        const Dec d = decode(v[i]);
+        const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
+        Q += q * q;
+      }
+    }
+  } else {
+    for (int h = threadIdx.x; h < k; h += kThreads) {
+      const Dec d = decode(__ldg(x + h));
+      const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
+      Q += q * q;
+    }
   }
   block_sum128(Q, Qhi, s_u64);
   if (threadIdx.x == 0)
