@@ -623,3 +623,18 @@ def test_accurate_bound_segments(N, k):
     ref = orc.gemm_entries(A, Bt, N, rows, cols, mode=orc.ACCURATE, want_X=False, want_c=False,
                            want_G=False)
     assert_bits_equal(C[np.ix_(rows, cols)], ref.C, f"accurate k={k}")
+
+
+@pytest.mark.parametrize("m,n,k", [(70000, 20, 40), (3, 70000, 40)])
+def test_tall_and_wide_shapes(m, n, k):
+    """More than 65535 rows of A or columns of B: the residue and CRT grids cap
+    their y dimension and loop, and m = 70000 runs the most row panels (8)."""
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=m + n, phi=1.0)
+    for mode, om in (("fast", orc.FAST), ("accurate", orc.ACCURATE)):
+        C = os2.gemm(dev(A), dev(Bt), 14, mode).cpu().numpy()
+        status_ok()
+        rows, cols = workloads.sample_grid(m, n, 16, seed=5)
+        ref = orc.gemm_entries(A, Bt, 14, rows, cols, mode=om, want_X=False, want_c=False,
+                               want_G=False)
+        assert ref.mismatches == 0
+        assert_bits_equal(C[np.ix_(rows, cols)], ref.C, f"{m}x{n}x{k} {mode}")
