@@ -212,19 +212,22 @@ os2_status os2_set_gemm_variant(int variant);
 /* Static description of a status code. */
 const char *os2_status_string(int status);
 
-/* Number of kernels os2_gemm launches for these arguments (for launch
- * accounting); 0 on bad args. */
+/* Number of kernels os2_gemm launches for these arguments with the step-3
+ * kernel currently selected (for launch accounting); 0 on bad args. */
 int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode);
 
-/* Per-kernel timing of os2_gemm / os2_gemm_host (a measurement aid; the pages
- * define no such call).  os2_profile_start() enables it: every kernel those
- * calls enqueue is then bracketed by two CUDA events on the caller's stream.
- * os2_profile_stop() disables it, waits for the recorded events, and writes
- * up to max_kernels aggregated entries: names[i*32..] (NUL-terminated kernel
- * role: scale_residue_A, scale_residue_B, gemm_bound, gemm_modp, crt_unscale),
- * total_ms[i] and launches[i].  Returns the entry count, or -1 if an event
- * failed.  Any output pointer may be NULL.  Process-wide, not thread-safe
- * against concurrent os2_gemm calls on other threads. */
+/* Per-kernel timing of os2_gemm / os2_gemm_host and the other whole-path
+ * entry points (a measurement aid; the pages define no such call).
+ * os2_profile_start() enables it: every kernel (or group of panel launches)
+ * those calls enqueue is then bracketed by two CUDA events on the stream it
+ * runs on (the caller's stream or one of the library's side streams, where a
+ * span includes the time it waits beside other work).  os2_profile_stop()
+ * disables it, waits for the recorded events, and writes up to max_kernels
+ * aggregated entries: names[i*32..] (NUL-terminated role: scale, scale_bars,
+ * gemm_bound, residues, gemm_modp, crt_unscale, complex_stack,
+ * complex_unstack), total_ms[i] and launches[i] (spans recorded).  Returns
+ * the entry count, or -1 if an event failed.  Any output pointer may be NULL.
+ * Process-wide, not thread-safe against concurrent calls on other threads. */
 os2_status os2_profile_start(void);
 int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launches);
 
