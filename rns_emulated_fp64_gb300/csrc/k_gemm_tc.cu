@@ -401,24 +401,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 // -------------------------------------------------------------------------
 // 2-SM variant of KIND 0: a CTA pair (cluster of 2) computes a 256x256 tile
 // with tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA loads 128
-// rows of the A tile and 128 rows of the B tile (its half of N) into a
-// 6-stage ring; both CTAs' copies complete on the even CTA's "full" barrier,
+// rows of the A tile and 128 rows of the B tile (its half of N) into a ring
+// of 3 stages of two k-blocks; both CTAs' copies complete on the even CTA's
+// "full" barrier,
 // the MMA commits are multicast to both CTAs' "empty" and "accumulator full"
 // barriers, and both CTAs' epilogues release an accumulator on the even
 // CTA's "accumulator empty" barrier.  Each CTA's TMEM holds its 128 rows x
-// 256 columns of the two interleaved jobs, reduced mod p exactly as in the
-// single-SM kernel.  Per SM this halves the B-tile traffic and lengthens the
-// operand lookahead from 2048 to 3072 MMA cycles.
-constexpr int kStages2 = 6;
+// 256 columns of the two interleaved jobs, reduced mod p like the single-SM
+// kernel's (with FMA-only rounding, see above).  Chunks are counted in stages:
+// at most 7 stages (896 terms) between reductions.  Per SM this halves the
+// B-tile traffic of the single-SM kernel.
+// A stage holds two k-blocks (128 terms): one operand wait, fence and commit
+// per eight MMAs instead of per four.
+constexpr int kStages2 = 3;
 constexpr int kHalf = 128;
+constexpr int BK2 = 2 * BK;  // terms per stage of the 2-SM kernel
+
+// ---------------------------------------------- 2-SM epilogue arithmetic
+// Accumulators hold exact integers |x| < 2^24.  Adding 1.5 * 2^23 rounds a
+// value of magnitude < 2^22 to an integer (ties to even) in the FMA's single
+// rounding, so x - p * round(x * fl(1/p)) takes three full-rate FP32 ops.
+constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+
+// An exact integer congruent to x mod p, of magnitude <= p/2 + 1:
+// |x * fl(1/p) - x / p| <= |x| * 2^-32 < 2^-8 for 128 < p <= 256.
+__device__ __forceinline__ float reduce_near(float x, float p, float invp) {
+  const float q = fmaf(x, invp, kRound) - kRound;
+  return fmaf(-p, q, x);
+}
+
+// The low byte of the symmetric residue of x.  After one step |r| <= p/2 + 1;
+// a second step moves the extremes +-(p+1)/2 of an odd p into range and leaves
+// the rest; for p = 256 the values +-128 share the byte 0x80.  r + 1.5 * 2^23
+// is exact and carries r mod 256 in its low byte.
+__device__ __forceinline__ uint32_t residue_byte(float x, float p, float invp) {
+  const float r = reduce_near(reduce_near(x, p, invp), p, invp);
+  return __float_as_uint(r + kRound);
+}
+
+// Low bytes of a, b, c, d packed into one word (a in the lowest byte).
+__device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
 
 // Accurate-mode bound product on the 2-SM kernel (BOUND = 1): one launch per
-// segment of at most 64 k-blocks, whose FP32 sums (Abar, Bbar <= 64, so each
+// segment of at most 32 stages (4096 terms), whose FP32 sums (Abar, Bbar <= 64, so each
 // product <= 2^12 and a segment's sum <= 2^24) are exact.  Segments after the
 // first add the int32 partial sums of the earlier ones; the last takes the
 // row and column maxima.
 struct BoundSeg {
-  int kb_begin;          // first k-block of the segment
+  int kb_begin;          // first stage (pair of k-blocks) of the segment
   int first, last;       // segment flags
   int32_t *partial;      // int32 [m][ldp] partial sums between segments
   int ldp;
@@ -496,7 +528,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                const Sched sp, const GemmConsts gc, int8_t *__restrict__ out, int ldo,
                const BoundSeg bs, int *status) {
   constexpr int BN = 256, STAGES = kStages2;
-  constexpr uint32_t A_BYTES = kHalf * BK * 2, B_BYTES = kHalf * BK * 2;
+  constexpr uint32_t HALF = kHalf * BK * 2;  // one k-block of 128 rows
+  constexpr uint32_t A_BYTES = 2 * HALF, B_BYTES = 2 * HALF;
   constexpr uint32_t IDESC = idesc_f16_f32(2 * kHalf, BN);
   constexpr uint32_t TMEM_COLS = 512;
 
@@ -561,11 +594,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
-          const int kx = (BOUND ? bs.kb_begin + kb : kb) * BK;
-          tma_load_3d_pair(sA + stage * A_BYTES, &mapA, fbar, kx,
-                           tm * 2 * kHalf + (int)rank * kHalf, l);
-          tma_load_3d_pair(sB + stage * B_BYTES, &mapB, fbar, kx,
-                           tn * BN + (int)rank * kHalf, l);
+          // a stage past the last k-block reads zeros (out-of-range box)
+          const int kx = (BOUND ? bs.kb_begin + kb : kb) * BK2;
+#pragma unroll
+          for (int h = 0; h < 2; h++) {
+            tma_load_3d_pair(sA + stage * A_BYTES + h * HALF, &mapA, fbar, kx + h * BK,
+                             tm * 2 * kHalf + (int)rank * kHalf, l);
+            tma_load_3d_pair(sB + stage * B_BYTES + h * HALF, &mapB, fbar, kx + h * BK,
+                             tn * BN + (int)rank * kHalf, l);
+          }
           used |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -605,12 +642,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             return false;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_k128(smem_u32(sA + stage * A_BYTES));
-          const uint64_t bd = sdesc_k128(smem_u32(sB + stage * B_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; kk++) {
-            const uint32_t acc = (kb > kb0 || kk > 0 || c > 0) ? 1u : 0u;
-            umma2_f16(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
+          for (int h = 0; h < 2; h++) {
+            const uint64_t ad = sdesc_k128(smem_u32(sA + stage * A_BYTES + h * HALF));
+            const uint64_t bd = sdesc_k128(smem_u32(sB + stage * B_BYTES + h * HALF));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; kk++) {
+              const uint32_t acc = (kb > kb0 || h > 0 || kk > 0 || c > 0) ? 1u : 0u;
+              umma2_f16(d, ad + 2 * kk, bd + 2 * kk, IDESC, acc);
+            }
           }
           umma2_commit_mc(&empty[stage], 0x3);
           if (++stage == STAGES) {
@@ -651,21 +691,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bound_epilogue(taddr, tm * 2 * kHalf + (int)rank * kHalf + r_in_tile, tn * BN, lane, sp,
                        bs);
       } else if (c != sp.nchunks - 1) {
+        // intermediate chunk: reduce in place (|r| <= p/2 + 1 carries into the next chunk)
 #pragma unroll 1
         for (int g = 0; g < BN / 32; g++) {
           uint32_t v[32];
           tmem_ld32(taddr + g * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i++) {
-            const float x = __uint_as_float(v[i]);
-            v[i] = __float_as_uint(fmaf(-p, rintf(x * invp), x));
-          }
+          for (int i = 0; i < 32; i++)
+            v[i] = __float_as_uint(reduce_near(__uint_as_float(v[i]), p, invp));
           tmem_st32(taddr + g * 32, v);
         }
         tmem_wait_st();
       } else {
-        const float hi = gc.hi[l], lo = gc.lo[l];
+        // final chunk: canonical symmetric residues as int8
         const int grow = tm * 2 * kHalf + (int)rank * kHalf + r_in_tile;
         const int col0 = tn * BN;
         int8_t *dst = out + ((size_t)l * sp.m + grow) * (size_t)ldo + col0;
@@ -676,15 +715,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           uint32_t packed[8];
 #pragma unroll
-          for (int i = 0; i < 8; i++) packed[i] = 0;
-#pragma unroll
-          for (int i = 0; i < 32; i++) {
-            const float x = __uint_as_float(v[i]);
-            float r = fmaf(-p, rintf(x * invp), x);
-            r = r > hi ? r - p : r;
-            r = r < lo ? r + p : r;
-            packed[i >> 2] |= ((uint32_t)(int)r & 0xFFu) << (8 * (i & 3));
-          }
+          for (int i = 0; i < 8; i++)
+            packed[i] = pack4(residue_byte(__uint_as_float(v[4 * i]), p, invp),
+                              residue_byte(__uint_as_float(v[4 * i + 1]), p, invp),
+                              residue_byte(__uint_as_float(v[4 * i + 2]), p, invp),
+                              residue_byte(__uint_as_float(v[4 * i + 3]), p, invp));
           if (grow < sp.m) {
             const int cb = col0 + g * 32;
             if (cb + 32 <= sp.n) {
@@ -692,8 +727,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               d4[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
               d4[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
             } else {
-              for (int i = 0; i < 32 && cb + i < sp.n; i++)
-                dst[g * 32 + i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+#pragma unroll
+              for (int i = 0; i < 32; i++)  // static indices keep `packed` in registers
+                if (cb + i < sp.n) dst[g * 32 + i] = (int8_t)((packed[i >> 2] >> (8 * (i & 3))) & 0xFFu);
             }
           }
         }
@@ -792,7 +828,7 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
 
 template <int BOUND>
 cudaError_t set_smem2() {
-  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
+  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * 2 * kHalf * BK * 2 + 256;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -816,15 +852,16 @@ Sched sched2(int m, int n, int kb_total, int nplanes) {
 
 cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
                     int ldo, const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows) {
-  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
+  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * 2 * kHalf * BK * 2 + 256;
   cudaError_t attr_err = set_smem2<0>();
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
   if (!make_map(&ma, RA, kp, m, nplanes, kHalf, m) ||
       !make_map(&mb, RB, kp, n, nplanes, kHalf, b_plane_rows))
     return cudaErrorInvalidValue;
-  Sched sp = sched2(m, n, kp / BK, nplanes);
-  sp.chunk = (int)(((1LL << 24) - 135) / ((long long)BK << 14));
+  // the 2-SM kernel counts k in stages of two k-blocks
+  Sched sp = sched2(m, n, (kp / BK + 1) / 2, nplanes);
+  sp.chunk = (int)(((1LL << 24) - 135) / ((long long)BK2 << 14));
   sp.nchunks = (sp.kb_total + sp.chunk - 1) / sp.chunk;
   if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
   const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
@@ -839,14 +876,14 @@ cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int np
 cudaError_t launch2_bound(int m, int n, int kp, const void *RA, const void *RB, int32_t *partial,
                           int ldp, int32_t *rowmax, int32_t *colmax, int *status,
                           cudaStream_t s) {
-  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * kHalf * BK * 2 + 256;
-  constexpr int kSegMax = (int)((1LL << 24) / ((long long)BK << 12));  // 64 k-blocks
+  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * 2 * kHalf * BK * 2 + 256;
+  constexpr int kSegMax = (int)((1LL << 24) / ((long long)BK2 << 12));  // 32 stages, 4096 terms
   cudaError_t attr_err = set_smem2<1>();
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
   if (!make_map(&ma, RA, kp, m, 1, kHalf, m) || !make_map(&mb, RB, kp, n, 1, kHalf, n))
     return cudaErrorInvalidValue;
-  const int kb_all = kp / BK;
+  const int kb_all = (kp / BK + 1) / 2;
   const int segs = (kb_all + kSegMax - 1) / kSegMax;
   if (segs > 1 && (!partial || ldp < n || ldp % 4 != 0 ||
                    (reinterpret_cast<uintptr_t>(partial) & 15)))
