@@ -133,11 +133,24 @@ void build_tables(int N, Os2Tables *t) {
     t->res.invp[l] = t->gemm.invp[l] = 1.0f / fp;
     t->res.hi[l] = t->gemm.hi[l] = hi;
     t->res.lo[l] = t->gemm.lo[l] = lo;
-    int pw = 1;
-    for (int u = 0; u < 7; u++) {
-      t->res.w12[l][u] = (float)sym(pw, p);
-      pw = (int)(((long long)pw * 4096) % p);
+    auto twice = [](float f) {
+      uint32_t u;
+      memcpy(&u, &f, 4);
+      return ((unsigned long long)u << 32) | u;
+    };
+    int c15[6], pw = 1;
+    for (int u = 0; u < 6; u++) {
+      c15[u] = sym(pw, p);
+      t->res.w15x2[l][u] = twice((float)c15[u]);
+      pw = (int)(((long long)pw * 32768) % p);
     }
+    for (int nw = 4; nw <= 6; nw++) {
+      int ks = 0;
+      for (int u = 0; u < nw - 1; u++) ks = (ks + 16384 * c15[u]) % p;
+      t->res.k15x2[l][nw - 4] = twice((float)sym(ks, p));
+    }
+    t->res.invp2[l] = twice(1.0f / fp);
+    t->res.negp2[l] = twice(-fp);
     for (int v = 0; v < 5; v++) t->crt.W32[l][v] = W.w[v];
   }
   for (int v = 0; v < 6; v++) {

@@ -19,7 +19,13 @@ struct ResConsts {
   float invp[OS2_MAX_MODULI];    // fl(1/p_l)
   float hi[OS2_MAX_MODULI];      // ceil(p_l/2) - 1   (top of the symmetric range)
   float lo[OS2_MAX_MODULI];      // -floor(p_l/2)     (bottom)
-  float w12[OS2_MAX_MODULI][7];  // symmetric residue of 2^(12 t) mod p_l, t = 0..6
+  // Step 2 word constants, each float twice in 64 bits (packed FP32 pairs):
+  // w15x2: symmetric residue of 2^(15 t) mod p_l, t = 0..5; k15x2[l][NW - 4]:
+  // symmetric residue of 2^14 (1 + 2^15 + ... + 2^(15 (NW - 2))) mod p_l.
+  unsigned long long w15x2[OS2_MAX_MODULI][6];
+  unsigned long long k15x2[OS2_MAX_MODULI][3];
+  unsigned long long invp2[OS2_MAX_MODULI];  // fl(1/p_l)
+  unsigned long long negp2[OS2_MAX_MODULI];  // -p_l
   uint32_t H[OS2_H_LIMBS];       // H = floor((P-1)/2), little-endian 32-bit limbs
   int bitlenH;
 };

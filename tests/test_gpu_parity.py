@@ -84,19 +84,36 @@ def test_residue_planes_parity(N, kind, phi):
 
 
 def test_residues_extreme_exponents():
-    """Exponents far from the fast-mode choice exercise every word of the
-    integer split (|A'| just below 2^84) and deep right shifts."""
+    """Exponents far from the fast-mode choice exercise every word count of
+    the integer split: integers just below and just above 2^59 and 2^74 (the
+    limits of four and five 15-bit words), up to just below 2^89, and deep
+    right shifts."""
     rng = np.random.default_rng(11)
     X = rng.standard_normal((40, 64))
+    X[7, 5] = -X[7, 5]
     E = int(np.frexp(np.abs(X).max())[1])          # |x| < 2^E
-    for N in (5, 20):
-        for e_val in (-60, -1, 0, 30, 83 - E):
+    for N in (5, 18, 20):
+        for e_val in (-60, -1, 0, 30, 59 - E, 60 - E, 74 - E, 75 - E, 83 - E, 89 - E):
             e = np.full(40, e_val, np.int32)
             planes = os2.residues(dev(X), dev(e), N)
             status_ok()
             want = orc.residues(X, e, N)
             assert np.array_equal(planes.cpu().numpy()[:, :, :64].astype(np.int64),
-                                  want.astype(np.int64))
+                                  want.astype(np.int64)), (N, e_val)
+
+
+def test_residues_integer_too_wide_is_reported():
+    """An exponent that makes |trunc(x 2^e)| reach 2^89 (beyond every
+    exponent step 1 produces) sets the range status instead of writing wrong
+    residues."""
+    X = np.full((2, 64), 0.75)                     # |x| < 2^0
+    e = np.array([90, 88], np.int32)               # row 0: 0.75 * 2^90 >= 2^89
+    planes = os2.residues(dev(X), dev(e), 3)
+    assert os2.get_status() == os2.binding.ERR_RANGE
+    status_ok()                                    # get_status cleared it
+    want = orc.residues(X[1:], e[1:], 3)
+    assert np.array_equal(planes.cpu().numpy()[:, 1, :64].astype(np.int64),
+                          want[:, 0].astype(np.int64))
 
 
 # ------------------------------------------------------------------ step 3 --
