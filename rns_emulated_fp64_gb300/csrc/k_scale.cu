@@ -179,6 +179,78 @@ struct RowSet {
 };
 
 // ------------------------------------------------------------- row scale ---
+// Monotone integer keys of |x| and the ceilings of steps 1 and 1A for rows
+// that hold at least one normal number and no Inf or NaN (every other row
+// takes the exact decode above).  key(x) = the high word of |x|'s bits, whose
+// maximum over a row gives the row's largest exponent field, so
+// E = (key >> kMantHi) - kEBias is the tight bound |x| < 2^E.
+template <typename T> struct FBits;
+template <> struct FBits<double> {
+  static constexpr uint32_t kInfKey = 0x7FF00000u, kNormKey = 0x00100000u;
+  static constexpr int kMantHi = 20, kEBias = 1022;
+  static __device__ __forceinline__ uint32_t key(double x) {
+    return (uint32_t)__double2hiint(x) & 0x7FFFFFFFu;
+  }
+  // ceil(|x| 2^(S - E)) for finite x with |x| < 2^E and E >= -1021: the
+  // significand m shifted right by r = E - S - ex2 >= 30 (S <= 23), taken as
+  // ((m - 1) >> r) + 1.
+  template <int S>
+  static __device__ __forceinline__ uint32_t ceil_scaled(double x, int E) {
+    const uint32_t hi = (uint32_t)__double2hiint(x), lo = (uint32_t)__double2loint(x);
+    const uint32_t bexp = (hi >> 20) & 0x7FFu;
+    const uint32_t mh = (hi & 0xFFFFFu) | (bexp ? 0x100000u : 0u);
+    if ((mh | lo) == 0u) return 0u;
+    const int r = E - S + 1075 - (int)max(bexp, 1u);
+    const uint32_t mlo = lo - 1u, mhi = mh - (lo == 0u ? 1u : 0u);
+    const uint32_t t = r < 32 ? __funnelshift_rc(mlo, mhi, (unsigned)r)
+                              : __funnelshift_rc(mhi, 0u, (unsigned)(r - 32));
+    return t + 1u;
+  }
+};
+template <> struct FBits<float> {
+  static constexpr uint32_t kInfKey = 0x7F800000u, kNormKey = 0x00800000u;
+  static constexpr int kMantHi = 23, kEBias = 126;
+  static __device__ __forceinline__ uint32_t key(float x) {
+    return __float_as_uint(x) & 0x7FFFFFFFu;
+  }
+  template <int S>
+  static __device__ __forceinline__ uint32_t ceil_scaled(float x, int E) {
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t bexp = (b >> 23) & 0xFFu;
+    const uint32_t m = (b & 0x7FFFFFu) | (bexp ? 0x800000u : 0u);
+    if (m == 0u) return 0u;
+    const int r = E - S + 150 - (int)max(bexp, 1u);  // >= 1 for S <= 23
+    return __funnelshift_rc(m - 1u, 0u, (unsigned)r) + 1u;
+  }
+};
+
+// Calls f on each of the thread's entries of a row (strided by the CTA),
+// with U two-entry vector loads in flight before the first use.  Entries past
+// k are passed as zero.
+template <typename T, typename F>
+__device__ __forceinline__ void for_row(const T *x, int k, bool vec, F &&f) {
+  if (vec) {
+    constexpr int U = 4;
+    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kThreads * U) {
+      T v[2 * U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int h = h0 + u * 2 * kThreads;
+        if (h + 1 < k) {
+          load2(x + h, v[2 * u], v[2 * u + 1]);
+        } else {
+          v[2 * u] = h < k ? __ldg(x + h) : T(0);
+          v[2 * u + 1] = T(0);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 2 * U; i++) f(v[i]);
+    }
+  } else {
+    for (int h = threadIdx.x; h < k; h += kThreads) f(__ldg(x + h));
+  }
+}
+
 template <int MODE, typename T>
 __global__ void __launch_bounds__(kThreads)
     k_row_scale(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
@@ -190,42 +262,30 @@ __global__ void __launch_bounds__(kThreads)
   const T *x = reinterpret_cast<const T *>(rs.X) + (size_t)row * rs.ldx;
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
 
-  // pass 1: exponent bound and finiteness
-  int emax = INT_MIN, bad = 0;
-  if (vec) {
-    // four independent 2-entry loads per thread in flight before any is used
-    constexpr int U = 4;
-    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kThreads * U) {
-      T v[2 * U];
-#pragma unroll
-      for (int u = 0; u < U; u++) {
-        const int h = h0 + u * 2 * kThreads;
-        if (h + 1 < k) {
-          load2(x + h, v[2 * u], v[2 * u + 1]);
-        } else {
-          v[2 * u] = h < k ? __ldg(x + h) : T(0);
-          v[2 * u + 1] = T(0);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 2 * U; i++) {
-        const Dec d = decode(v[i]);
-        bad |= d.nonfinite;
-        emax = max(emax, exp_bound(d));
-      }
-    }
+  // pass 1: the largest key of the row
+  uint32_t key = 0;
+  for_row(x, k, vec, [&](T v) { key = max(key, FBits<T>::key(v)); });
+  key = (uint32_t)block_max((int)key, s_int);
+  const bool general = key >= FBits<T>::kInfKey || key < FBits<T>::kNormKey;
+  int E, bad = 0;
+  bool nonzero = true;
+  if (!general) {
+    E = (int)(key >> FBits<T>::kMantHi) - FBits<T>::kEBias;
   } else {
-    for (int h = threadIdx.x; h < k; h += kThreads) {
-      const Dec d = decode(__ldg(x + h));
+    // Inf or NaN present, or no normal number: exponent bound and finiteness
+    // entry by entry
+    int emax = INT_MIN;
+    for_row(x, k, vec, [&](T v) {
+      const Dec d = decode(v);
       bad |= d.nonfinite;
       emax = max(emax, exp_bound(d));
-    }
+    });
+    emax = block_max(emax, s_int);
+    bad = block_max(bad, s_int);
+    if (bad && threadIdx.x == 0) set_status(status, OS2_ERR_NONFINITE);
+    nonzero = emax != INT_MIN;
+    E = nonzero ? emax : 0;
   }
-  emax = block_max(emax, s_int);
-  bad = block_max(bad, s_int);
-  if (bad && threadIdx.x == 0) set_status(status, OS2_ERR_NONFINITE);
-  const bool nonzero = emax != INT_MIN;
-  const int E = nonzero ? emax : 0;
 
   if (MODE == SM_BARS) {
     // accurate mode: E_i and Abar_ih = ceil(|a_ih| 2^(6 - E_i)) in [0, 64]
@@ -233,12 +293,25 @@ __global__ void __launch_bounds__(kThreads)
     __half *dst = rs.planes + (size_t)row * kp;
     for (int ch = threadIdx.x; ch < kp / 8; ch += kThreads) {
       const int h0 = ch * 8;
-      __align__(16) __half v[8];
+      T xv[8];
+      if (vec && h0 + 8 <= k) {
 #pragma unroll
-      for (int u = 0; u < 8; u++) {
-        const int h = h0 + u;
-        const Dec d = decode(h < k ? __ldg(x + h) : T(0));
-        v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
+        for (int u = 0; u < 4; u++) load2(x + h0 + 2 * u, xv[2 * u], xv[2 * u + 1]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; u++) xv[u] = h0 + u < k ? __ldg(x + h0 + u) : T(0);
+      }
+      __align__(16) __half v[8];
+      if (!general) {
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+          v[u] = __float2half_rn((float)FBits<T>::template ceil_scaled<6>(xv[u], E));
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+          const Dec d = decode(xv[u]);
+          v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
+        }
       }
       *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
     }
@@ -249,33 +322,17 @@ __global__ void __launch_bounds__(kThreads)
   // (each q^2 <= 2^46; a thread's partial stays below 2^64 for k < 2^26;
   // the block sum is 128-bit)
   unsigned long long Q = 0, Qhi = 0;
-  if (vec) {
-    constexpr int U = 4;
-    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kThreads * U) {
-      T v[2 * U];
-#pragma unroll
-      for (int u = 0; u < U; u++) {
-        const int h = h0 + u * 2 * kThreads;
-        if (h + 1 < k) {
-          load2(x + h, v[2 * u], v[2 * u + 1]);
-        } else {
-          v[2 * u] = h < k ? __ldg(x + h) : T(0);
-          v[2 * u + 1] = T(0);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 2 * U; i++) {
-        const Dec d = decode(v[i]);
-        const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
-        Q += q * q;
-      }
-    }
+  if (!general) {
+    for_row(x, k, vec, [&](T v) {
+      const uint32_t q = FBits<T>::template ceil_scaled<23>(v, E);
+      Q += (unsigned long long)q * q;
+    });
   } else {
-    for (int h = threadIdx.x; h < k; h += kThreads) {
-      const Dec d = decode(__ldg(x + h));
+    for_row(x, k, vec, [&](T v) {
+      const Dec d = decode(v);
       const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
       Q += q * q;
-    }
+    });
   }
   block_sum128(Q, Qhi, s_u64);
   if (threadIdx.x == 0)
