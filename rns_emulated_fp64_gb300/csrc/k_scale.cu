@@ -37,7 +37,8 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;       // residue kernel
+constexpr int kScaleThreads = 256;  // row scale kernel: one CTA per row
 
 struct Dec {
   uint64_t mant;  // |x| = mant * 2^ex2
@@ -120,13 +121,28 @@ __device__ bool fits(uint64_t Qlo, uint64_t Qhi, int g, const uint32_t *H) {
   return true;
 }
 // Largest integer g with Q * 4^g <= H, Q = Qhi 2^64 + Qlo >= 1.  With b(.)
-// the bit length, the answer is floor((b(H)+1-b(Q))/2) or one less.
+// the bit length and g0 = floor((b(H) + 1 - b(Q)) / 2), Q 4^g0 has b(H) + 1
+// bits (then g0 - 1 is the answer) or b(H) bits; in the second case the 64
+// leading bits of Q and of H decide, unless they are equal and both have set
+// bits below them (then the full comparison does).
 __device__ int largest_g(uint64_t Qlo, uint64_t Qhi, const ResConsts &c) {
   const int bQ = Qhi ? 128 - __clzll((long long)Qhi) : 64 - __clzll((long long)Qlo);
-  int g = (c.bitlenH + 1 - bQ) >> 1;
-  for (int it = 0; it < 3; it++, g--)
-    if (fits(Qlo, Qhi, g, c.H)) return g;
-  return g;
+  const int g = (c.bitlenH + 1 - bQ) >> 1;
+  if (bQ + 2 * g > c.bitlenH) return g - 1;
+  uint64_t w;
+  bool rest;
+  if (bQ <= 64) {
+    w = Qlo << (64 - bQ);
+    rest = false;
+  } else {
+    const int s = bQ - 64;  // 1..64
+    w = s == 64 ? Qhi : (Qhi << (64 - s)) | (Qlo >> s);
+    rest = s == 64 ? Qlo != 0 : (Qlo & ((1ull << s) - 1)) != 0;
+  }
+  if (w != c.H64) return w < c.H64 ? g : g - 1;
+  if (!rest) return g;
+  if (!c.Hrest) return g - 1;
+  return fits(Qlo, Qhi, g, c.H) ? g : g - 1;
 }
 
 __device__ __forceinline__ int block_max(int v, int *sh) {
@@ -135,7 +151,7 @@ __device__ __forceinline__ int block_max(int v, int *sh) {
   __syncthreads();
   if (l == 0) sh[w] = v;
   __syncthreads();
-  v = l < (kThreads / 32) ? sh[l] : INT_MIN;
+  v = l < (kScaleThreads / 32) ? sh[l] : INT_MIN;
   for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
@@ -157,8 +173,8 @@ __device__ __forceinline__ void block_sum128(unsigned long long &lo, unsigned lo
     sh[2 * w + 1] = hi;
   }
   __syncthreads();
-  lo = l < (kThreads / 32) ? sh[2 * l] : 0ull;
-  hi = l < (kThreads / 32) ? sh[2 * l + 1] : 0ull;
+  lo = l < (kScaleThreads / 32) ? sh[2 * l] : 0ull;
+  hi = l < (kScaleThreads / 32) ? sh[2 * l + 1] : 0ull;
   for (int o = 16; o; o >>= 1)
     add128(lo, hi, __shfl_xor_sync(0xffffffffu, lo, o), __shfl_xor_sync(0xffffffffu, hi, o));
 }
@@ -231,11 +247,11 @@ template <typename T, typename F>
 __device__ __forceinline__ void for_row(const T *x, int k, bool vec, F &&f) {
   if (vec) {
     constexpr int U = 4;
-    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kThreads * U) {
+    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kScaleThreads * U) {
       T v[2 * U];
 #pragma unroll
       for (int u = 0; u < U; u++) {
-        const int h = h0 + u * 2 * kThreads;
+        const int h = h0 + u * 2 * kScaleThreads;
         if (h + 1 < k) {
           load2(x + h, v[2 * u], v[2 * u + 1]);
         } else {
@@ -247,12 +263,12 @@ __device__ __forceinline__ void for_row(const T *x, int k, bool vec, F &&f) {
       for (int i = 0; i < 2 * U; i++) f(v[i]);
     }
   } else {
-    for (int h = threadIdx.x; h < k; h += kThreads) f(__ldg(x + h));
+    for (int h = threadIdx.x; h < k; h += kScaleThreads) f(__ldg(x + h));
   }
 }
 
 template <int MODE, typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kScaleThreads)
     k_row_scale(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
   __shared__ int s_int[32];
   __shared__ unsigned long long s_u64[2 * 32];
@@ -291,7 +307,7 @@ __global__ void __launch_bounds__(kThreads)
     // accurate mode: E_i and Abar_ih = ceil(|a_ih| 2^(6 - E_i)) in [0, 64]
     if (threadIdx.x == 0) rs.E[row] = E;
     __half *dst = rs.planes + (size_t)row * kp;
-    for (int ch = threadIdx.x; ch < kp / 8; ch += kThreads) {
+    for (int ch = threadIdx.x; ch < kp / 8; ch += kScaleThreads) {
       const int h0 = ch * 8;
       T xv[8];
       if (vec && h0 + 8 <= k) {
@@ -544,11 +560,11 @@ cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int r
   RowSet b{XB, ldb, rowsB, eB, EB, reinterpret_cast<__half *>(barsB), rowsB};
   dim3 grid(rowsA + rowsB);
   if (mode == SM_BARS) {
-    if (f32) k_row_scale<SM_BARS, float><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
-    else k_row_scale<SM_BARS, double><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    if (f32) k_row_scale<SM_BARS, float><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    else k_row_scale<SM_BARS, double><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
   } else {
-    if (f32) k_row_scale<SM_FAST_SCALE, float><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
-    else k_row_scale<SM_FAST_SCALE, double><<<grid, kThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    if (f32) k_row_scale<SM_FAST_SCALE, float><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    else k_row_scale<SM_FAST_SCALE, double><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
   }
   return cudaGetLastError();
 }

@@ -164,6 +164,16 @@ void build_tables(int N, Os2Tables *t) {
   t->crt.s128 = (float)(128.0 / Pd);
   for (int i = 0; i < OS2_H_LIMBS; i++) t->res.H[i] = H.w[i];
   t->res.bitlenH = u_bitlen(H);
+  {
+    const int bH = t->res.bitlenH;
+    auto bit = [&](int i) { return i >= 0 ? (H.w[i >> 5] >> (i & 31)) & 1u : 0u; };
+    unsigned long long w = 0;
+    for (int i = 0; i < 64; i++) w = (w << 1) | bit(bH - 1 - i);
+    int rest = 0;
+    for (int i = 0; i < bH - 64; i++) rest |= (int)bit(i);
+    t->res.H64 = w;
+    t->res.Hrest = rest;
+  }
 }
 
 std::atomic<int> g_variant{OS2_GEMM_TC};

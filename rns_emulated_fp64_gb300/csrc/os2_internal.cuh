@@ -28,6 +28,8 @@ struct ResConsts {
   unsigned long long negp2[OS2_MAX_MODULI];  // -p_l
   uint32_t H[OS2_H_LIMBS];       // H = floor((P-1)/2), little-endian 32-bit limbs
   int bitlenH;
+  unsigned long long H64;        // the 64 leading bits of H (leading bit at bit 63)
+  int Hrest;                     // nonzero if H has set bits below those 64
 };
 
 // Steps 4-5 constants (32-bit little-endian limbs).
