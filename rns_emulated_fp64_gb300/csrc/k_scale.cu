@@ -20,8 +20,8 @@
 //   k_row_scale  one CTA per row: exponent bound (pass 1), then either the
 //                fast-mode sum of squares and e_i, or the accurate-mode
 //                7-bit magnitude plane (pass 2 re-reads the row from L1/L2).
-//   k_residues   element-parallel: every thread turns 4 consecutive entries
-//                into 4 residues per modulus and writes one 8-byte vector to
+//   k_residues   element-parallel: every thread turns 8 consecutive entries
+//                into 8 residues per modulus and writes one 16-byte vector to
 //                each plane.  Residues of the odd moduli use FP32 arithmetic
 //                only: the integer is split into four to six 15-bit words w_t
 //                (as many as its size needs) and x = K + sum_t w_t (2^(15t)
@@ -488,7 +488,7 @@ __device__ __forceinline__ void residues_of(const T (&v)[EPT], int ee, const Res
 }
 
 // Residue planes: EPT consecutive entries per thread, one vector store per plane.
-constexpr int kEPT = 4;
+constexpr int kEPT = 8;
 
 template <int N, typename T>
 __global__ void __launch_bounds__(kThreads, 3)
