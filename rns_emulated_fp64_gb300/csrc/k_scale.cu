@@ -278,9 +278,26 @@ __global__ void __launch_bounds__(kScaleThreads)
   const T *x = reinterpret_cast<const T *>(rs.X) + (size_t)row * rs.ldx;
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
 
-  // pass 1: the largest key of the row
+  // pass 1: the largest key of the row.  For doubles only the high words are
+  // loaded, sixteen 4-byte loads per thread in flight: the same DRAM sectors
+  // as full loads, but twice the entries per register.
   uint32_t key = 0;
-  for_row(x, k, vec, [&](T v) { key = max(key, FBits<T>::key(v)); });
+  if (sizeof(T) == 8) {
+    constexpr int U = 16;
+    const uint32_t *xh = reinterpret_cast<const uint32_t *>(x) + 1;
+    for (int h0 = threadIdx.x; h0 < k; h0 += kScaleThreads * U) {
+      uint32_t hv[U];
+#pragma unroll
+      for (int u = 0; u < U; u++) {
+        const int h = h0 + u * kScaleThreads;
+        hv[u] = h < k ? __ldg(xh + 2 * (size_t)h) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; u++) key = max(key, hv[u] & 0x7FFFFFFFu);
+    }
+  } else {
+    for_row(x, k, vec, [&](T v) { key = max(key, FBits<T>::key(v)); });
+  }
   key = (uint32_t)block_max((int)key, s_int);
   const bool general = key >= FBits<T>::kInfKey || key < FBits<T>::kNormKey;
   int E, bad = 0;
