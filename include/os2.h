@@ -60,7 +60,7 @@ typedef enum {
   OS2_ERR_UNSUPPORTED = 2,  /* valid but beyond a documented size limit */
   OS2_ERR_WORKSPACE = 3,    /* workspace missing or smaller than os2_workspace_size */
   OS2_ERR_NONFINITE = 4,    /* an input entry is Inf or NaN (device-detected) */
-  OS2_ERR_RANGE = 5,        /* reserved: CRT bound violated (debug checks) */
+  OS2_ERR_RANGE = 5,        /* a scaled integer of os2_residues reached 2^89 */
   OS2_ERR_TIMEOUT = 6,      /* a device-side wait gave up (device-detected) */
   OS2_ERR_CUDA = 7          /* a CUDA runtime/driver call failed */
 } os2_status;
@@ -163,7 +163,10 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
 /* Step 2 alone for one operand: rows x k matrix X (row-major, ldx >= k; pass B
  * as its n columns), exponents exps (rows int32).  Writes N planes of FP16
  * symmetric residues, planes[(l*rows + r)*ldp + h] = sym(trunc(x_rh 2^exps_r) mod p_l),
- * for h < ldp; entries h >= k are written as 0.  ldp >= k, ldp % 64 == 0. */
+ * for h < ldp; entries h >= k are written as 0.  ldp >= k, ldp % 64 == 0.
+ * Every exponent os2_scale returns keeps |trunc(x 2^e)| below 2^84; hand-picked
+ * exponents that reach 2^89 set OS2_ERR_RANGE in the status word, and the
+ * residues of the 8-entry groups holding such entries are written as 0. */
 os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t *exps,
                         int num_moduli, void *planes, int ldp, void *stream);
 

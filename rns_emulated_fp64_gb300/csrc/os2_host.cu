@@ -998,7 +998,7 @@ const char *os2_status_string(int status) {
     case OS2_ERR_UNSUPPORTED: return "unsupported size or configuration";
     case OS2_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case OS2_ERR_NONFINITE: return "non-finite input entry";
-    case OS2_ERR_RANGE: return "CRT range exceeded";
+    case OS2_ERR_RANGE: return "scaled integer out of range (|trunc(x 2^e)| >= 2^89)";
     case OS2_ERR_TIMEOUT: return "device-side wait timed out";
     case OS2_ERR_CUDA: return "CUDA error";
   }
