@@ -493,10 +493,13 @@ def _f32_bits_equal(got, want, what):
 
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
 @pytest.mark.parametrize("N,m,n,k", [(7, 64, 64, 64), (4, 129, 257, 65), (8, 300, 200, 1000),
-                                     (10, 130, 140, 1921), (14, 33, 65, 3000)])
+                                     (10, 130, 140, 1921), (14, 33, 65, 3000), (18, 70, 90, 200),
+                                     (20, 64, 48, 100)])
 def test_sgemm_parity(mode, N, m, n, k):
     """SGEMM emulation ([G] Ergebnisse): float operands, binary32 result,
-    bit-exact against the oracle rounding the same CRT integer to binary32."""
+    bit-exact against the oracle rounding the same CRT integer to binary32.
+    At 18 and 20 moduli the scaled integers exceed 2^59, so step 2 takes its
+    five- and six-word paths on float input."""
     A, Bt = workloads.make_pair("spread", m, n, k, seed=N + k, phi=1.0)
     A = A.astype(np.float32)
     Bt = Bt.astype(np.float32)
