@@ -38,7 +38,8 @@
 namespace {
 
 constexpr int kThreads = 256;       // residue kernel
-constexpr int kScaleThreads = 256;  // row scale kernel: one CTA per row
+// Row scale kernel: one CTA of NT threads per row, NT = 256, 512 or 1024 as k
+// grows (see launch_row_scale).
 
 struct Dec {
   uint64_t mant;  // |x| = mant * 2^ex2
@@ -145,13 +146,14 @@ __device__ int largest_g(uint64_t Qlo, uint64_t Qhi, const ResConsts &c) {
   return fits(Qlo, Qhi, g, c.H) ? g : g - 1;
 }
 
+template <int NT>
 __device__ __forceinline__ int block_max(int v, int *sh) {
   for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();
   if (l == 0) sh[w] = v;
   __syncthreads();
-  v = l < (kScaleThreads / 32) ? sh[l] : INT_MIN;
+  v = l < (NT / 32) ? sh[l] : INT_MIN;
   for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
@@ -162,6 +164,7 @@ __device__ __forceinline__ void add128(unsigned long long &lo, unsigned long lon
   hi += bhi + (s < lo ? 1ull : 0ull);
   lo = s;
 }
+template <int NT>
 __device__ __forceinline__ void block_sum128(unsigned long long &lo, unsigned long long &hi,
                                              unsigned long long *sh) {
   for (int o = 16; o; o >>= 1)
@@ -173,8 +176,8 @@ __device__ __forceinline__ void block_sum128(unsigned long long &lo, unsigned lo
     sh[2 * w + 1] = hi;
   }
   __syncthreads();
-  lo = l < (kScaleThreads / 32) ? sh[2 * l] : 0ull;
-  hi = l < (kScaleThreads / 32) ? sh[2 * l + 1] : 0ull;
+  lo = l < (NT / 32) ? sh[2 * l] : 0ull;
+  hi = l < (NT / 32) ? sh[2 * l + 1] : 0ull;
   for (int o = 16; o; o >>= 1)
     add128(lo, hi, __shfl_xor_sync(0xffffffffu, lo, o), __shfl_xor_sync(0xffffffffu, hi, o));
 }
@@ -243,15 +246,15 @@ template <> struct FBits<float> {
 // Calls f on each of the thread's entries of a row (strided by the CTA),
 // with U two-entry vector loads in flight before the first use.  Entries past
 // k are passed as zero.
-template <typename T, typename F>
+template <int NT, typename T, typename F>
 __device__ __forceinline__ void for_row(const T *x, int k, bool vec, F &&f) {
   if (vec) {
     constexpr int U = 4;
-    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * kScaleThreads * U) {
+    for (int h0 = 2 * threadIdx.x; h0 < k; h0 += 2 * NT * U) {
       T v[2 * U];
 #pragma unroll
       for (int u = 0; u < U; u++) {
-        const int h = h0 + u * 2 * kScaleThreads;
+        const int h = h0 + u * 2 * NT;
         if (h + 1 < k) {
           load2(x + h, v[2 * u], v[2 * u + 1]);
         } else {
@@ -263,12 +266,12 @@ __device__ __forceinline__ void for_row(const T *x, int k, bool vec, F &&f) {
       for (int i = 0; i < 2 * U; i++) f(v[i]);
     }
   } else {
-    for (int h = threadIdx.x; h < k; h += kScaleThreads) f(__ldg(x + h));
+    for (int h = threadIdx.x; h < k; h += NT) f(__ldg(x + h));
   }
 }
 
-template <int MODE, typename T>
-__global__ void __launch_bounds__(kScaleThreads)
+template <int MODE, typename T, int NT>
+__global__ void __launch_bounds__(NT, 2048 / NT)
     k_row_scale(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
   __shared__ int s_int[32];
   __shared__ unsigned long long s_u64[2 * 32];
@@ -285,20 +288,20 @@ __global__ void __launch_bounds__(kScaleThreads)
   if (sizeof(T) == 8) {
     constexpr int U = 16;
     const uint32_t *xh = reinterpret_cast<const uint32_t *>(x) + 1;
-    for (int h0 = threadIdx.x; h0 < k; h0 += kScaleThreads * U) {
+    for (int h0 = threadIdx.x; h0 < k; h0 += NT * U) {
       uint32_t hv[U];
 #pragma unroll
       for (int u = 0; u < U; u++) {
-        const int h = h0 + u * kScaleThreads;
+        const int h = h0 + u * NT;
         hv[u] = h < k ? __ldg(xh + 2 * (size_t)h) : 0u;
       }
 #pragma unroll
       for (int u = 0; u < U; u++) key = max(key, hv[u] & 0x7FFFFFFFu);
     }
   } else {
-    for_row(x, k, vec, [&](T v) { key = max(key, FBits<T>::key(v)); });
+    for_row<NT>(x, k, vec, [&](T v) { key = max(key, FBits<T>::key(v)); });
   }
-  key = (uint32_t)block_max((int)key, s_int);
+  key = (uint32_t)block_max<NT>((int)key, s_int);
   const bool general = key >= FBits<T>::kInfKey || key < FBits<T>::kNormKey;
   int E, bad = 0;
   bool nonzero = true;
@@ -308,13 +311,13 @@ __global__ void __launch_bounds__(kScaleThreads)
     // Inf or NaN present, or no normal number: exponent bound and finiteness
     // entry by entry
     int emax = INT_MIN;
-    for_row(x, k, vec, [&](T v) {
+    for_row<NT>(x, k, vec, [&](T v) {
       const Dec d = decode(v);
       bad |= d.nonfinite;
       emax = max(emax, exp_bound(d));
     });
-    emax = block_max(emax, s_int);
-    bad = block_max(bad, s_int);
+    emax = block_max<NT>(emax, s_int);
+    bad = block_max<NT>(bad, s_int);
     if (bad && threadIdx.x == 0) set_status(status, OS2_ERR_NONFINITE);
     nonzero = emax != INT_MIN;
     E = nonzero ? emax : 0;
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(kScaleThreads)
     // accurate mode: E_i and Abar_ih = ceil(|a_ih| 2^(6 - E_i)) in [0, 64]
     if (threadIdx.x == 0) rs.E[row] = E;
     __half *dst = rs.planes + (size_t)row * kp;
-    for (int ch = threadIdx.x; ch < kp / 8; ch += kScaleThreads) {
+    for (int ch = threadIdx.x; ch < kp / 8; ch += NT) {
       const int h0 = ch * 8;
       T xv[8];
       if (vec && h0 + 8 <= k) {
@@ -356,18 +359,18 @@ __global__ void __launch_bounds__(kScaleThreads)
   // the block sum is 128-bit)
   unsigned long long Q = 0, Qhi = 0;
   if (!general) {
-    for_row(x, k, vec, [&](T v) {
+    for_row<NT>(x, k, vec, [&](T v) {
       const uint32_t q = FBits<T>::template ceil_scaled<23>(v, E);
       Q += (unsigned long long)q * q;
     });
   } else {
-    for_row(x, k, vec, [&](T v) {
+    for_row<NT>(x, k, vec, [&](T v) {
       const Dec d = decode(v);
       const unsigned long long q = ceil_shift(d.mant, d.ex2 + 23 - E);
       Q += q * q;
     });
   }
-  block_sum128(Q, Qhi, s_u64);
+  block_sum128<NT>(Q, Qhi, s_u64);
   if (threadIdx.x == 0)
     rs.e[row] = (nonzero && !bad && (Q | Qhi)) ? largest_g(Q, Qhi, c) + 23 - E : 0;
 }
@@ -576,13 +579,22 @@ cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int r
   RowSet a{XA, lda, rowsA, eA, EA, reinterpret_cast<__half *>(barsA), rowsA};
   RowSet b{XB, ldb, rowsB, eB, EB, reinterpret_cast<__half *>(barsB), rowsB};
   dim3 grid(rowsA + rowsB);
+  // About 32 entries per thread: the rows in flight (2048 threads per SM) then
+  // hold about 80 MB of doubles whatever k is, so the second pass over each
+  // row still finds it in L2.
+  const int nt = k > 16384 ? 1024 : (k > 8192 ? 512 : 256);
+#define OS2_SCALE(M, T)                                                                    \
+  (nt == 1024  ? (k_row_scale<M, T, 1024><<<grid, 1024, 0, s>>>(a, b, k, kp, t->res, status), 0) \
+   : nt == 512 ? (k_row_scale<M, T, 512><<<grid, 512, 0, s>>>(a, b, k, kp, t->res, status), 0)   \
+               : (k_row_scale<M, T, 256><<<grid, 256, 0, s>>>(a, b, k, kp, t->res, status), 0))
   if (mode == SM_BARS) {
-    if (f32) k_row_scale<SM_BARS, float><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
-    else k_row_scale<SM_BARS, double><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    if (f32) OS2_SCALE(SM_BARS, float);
+    else OS2_SCALE(SM_BARS, double);
   } else {
-    if (f32) k_row_scale<SM_FAST_SCALE, float><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
-    else k_row_scale<SM_FAST_SCALE, double><<<grid, kScaleThreads, 0, s>>>(a, b, k, kp, t->res, status);
+    if (f32) OS2_SCALE(SM_FAST_SCALE, float);
+    else OS2_SCALE(SM_FAST_SCALE, double);
   }
+#undef OS2_SCALE
   return cudaGetLastError();
 }
 
