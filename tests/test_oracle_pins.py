@@ -152,6 +152,25 @@ def test_oracle_residues_match_python():
             assert ints[i, h] == bigref.trunc_scaled(float(A[i, h]), int(e[i]))
 
 
+def test_oracle_residues_of_wide_integers():
+    """Residues of integers up to just below 2^89 (the widest the GPU tests
+    give the residue step) against Python's exact truncation and modulo."""
+    rng = np.random.default_rng(12)
+    X = rng.standard_normal((5, 16))
+    X[1, 3] = -X[1, 3]
+    E = int(np.frexp(np.abs(X).max())[1])          # |x| < 2^E
+    mods = orc.moduli(20)
+    for e_val in (59 - E, 60 - E, 74 - E, 75 - E, 88 - E, 89 - E):
+        e = np.full(5, e_val, np.int32)
+        res = orc.residues(X, e, 20)
+        for i in range(5):
+            for h in range(16):
+                a = bigref.trunc_scaled(float(X[i, h]), e_val)
+                assert abs(a) < 2 ** 89
+                for l, p in enumerate(mods):
+                    assert res[l, i, h] == bigref.sym(a, p), (e_val, i, h, p)
+
+
 # ------------------------------------------------------------ scaling -------
 def _exact_sq(row):
     return sum(Fraction(x) ** 2 for x in row)
