@@ -59,6 +59,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the N in {14,16,18} x {fast, accurate} sweep of the same workload")
+    ap.add_argument("--no-peaks", action="store_true",
+                    help="skip the tensor-pipe peak probes (own kernels) before the timed steps")
+    ap.add_argument("--peaks-only", action="store_true",
+                    help="run only the tensor-pipe peak probes and print them as one JSON line")
     return ap.parse_args()
 
 
@@ -208,6 +212,58 @@ def aggregate(world, ms_local, flop_per_step_per_rank, steps, device="cuda"):
     return ms_max, world * flop_per_step_per_rank * steps / (ms_max / 1e3) / 1e12
 
 
+# ------------------------------------------------------- pipe peak probes ---
+PROBES = (("tcgen05_f16_2sm", "PROBE_F16_2SM", "TFLOP/s"),
+          ("tcgen05_f16_1sm", "PROBE_F16_1SM", "TFLOP/s"),
+          ("mma_sync_s8", "PROBE_S8_SYNC", "TOPS"))
+
+
+def pipe_peaks(os2, stream, uuid, target_ms=30.0, reps=5):
+    """Throughput ceilings of the tensor-core instructions the library can use,
+    from its own self-checking probe kernels (os2_peak_probe): a check run
+    (exact result compared on the CUDA cores), then `reps` timed launches of
+    about `target_ms` each, CUDA events on the launching stream.  Reported:
+    the best and median launch, and the same per SM clock cycle at the median
+    sampled SM clock."""
+    import torch
+    out = {}
+    clocks = ClockSampler(uuid)
+    time.sleep(0.2)
+    for name, const, unit in PROBES:
+        kind = getattr(os2, const)
+        _, bad, ctas = os2.peak_probe(kind, 64, check=True, stream=stream)
+        if os2.get_status(stream):
+            raise RuntimeError(f"device status set by the {name} probe")
+        # size the launch from a short one
+        it0 = 2000
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        os2.peak_probe(kind, it0, stream=stream)
+        e0.record(stream)
+        os2.peak_probe(kind, it0, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iters = max(it0, int(it0 * target_ms / max(e0.elapsed_time(e1), 1e-3)))
+        rates = []
+        for _ in range(reps):
+            e0.record(stream)
+            fl = os2.peak_probe(kind, iters, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            rates.append(fl / (e0.elapsed_time(e1) / 1e3) / 1e12)
+        if os2.get_status(stream):
+            raise RuntimeError(f"device status set by the {name} probe")
+        out[name] = {"best": max(rates), "median": statistics.median(rates), "unit": unit,
+                     "iters": iters, "check_mismatches": bad, "ctas_checked": ctas}
+    clk = clocks.stop()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = clk.get("sm_mhz")
+    for v in out.values():
+        if mhz:
+            v["flop_per_sm_cycle_at_median_clock"] = v["median"] * 1e12 / (sms * mhz * 1e6)
+    out["clocks"] = clk
+    return out
+
+
 # ------------------------------------------------------------ CPU oracle ---
 def oracle_sample(A, Bt, a, seconds, rows_cols=None):
     """Time the oracle on a growing grid of output entries until `seconds`
@@ -280,15 +336,16 @@ def run_ours(a):
     def step():
         os2.gemm(Ad, Bd, N, a.mode, out=Cd, workspace=ws, stream=stream)
 
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    if not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    peaks_probe = None if a.no_peaks else pipe_peaks(os2, stream, uuid)
+
     for _ in range(a.warmup):
         step()
     st = os2.get_status(stream)
     if st:
         raise RuntimeError(f"device status after warm-up: {os2.status_string(st)}")
-
-    uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    if not uuid.startswith("GPU-"):
-        uuid = "GPU-" + uuid
     clocks = ClockSampler(uuid)
     time.sleep(0.3)
     barrier(world)
@@ -342,15 +399,28 @@ def run_ours(a):
                 v["achieved"] = work / secs / 1e12
                 v["unit"] = "TFLOP/s"
     g = kern.get("gemm_modp")
-    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    # the burst peak for a timed region shorter than a few seconds, the
+    # sustained (power-capped) one for a region that lasts seconds
+    timed_s = ms / 1e3
+    sustained = timed_s >= 3.0 and "bf16_tflops_sustained" in peaks
+    peak_t = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     roofline = None
     if g:
         roofline = {"bound": "tensor", "kernel": "gemm_modp (tcgen05.mma kind::f16, FP16-held residues)",
                     "achieved": g["achieved"], "peak": peak_t, "unit": "TFLOP/s",
                     "frac": g["achieved"] / peak_t, "traffic": kernel_traffic("gemm_modp"),
-                    "peak_source": f"{src} bf16 dense sustained (FP16 rate = BF16 rate)",
+                    "peak_source": "%s bf16 dense %s (of %s; FP16 rate = BF16 rate); timed region "
+                                   "%.2f s" % (src, "sustained" if sustained else "burst", src,
+                                               timed_s),
                     "work_per_launch": "N*2mnk / launches per step = %.4g flop"
                                        % (2.0 * N * m * n * k / max(g["launches_per_step"], 1.0))}
+        if peaks_probe:
+            own = peaks_probe["tcgen05_f16_2sm"]["best"]
+            roofline["own_pipe_peak"] = {
+                "kind_f16_2sm_tflops": own, "frac": g["achieved"] / own,
+                "int8_mma_sync_tops": peaks_probe["mma_sync_s8"]["best"],
+                "source": "os2_peak_probe, this run (self-checked, operands resident in "
+                          "shared memory)"}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True,
@@ -358,6 +428,8 @@ def run_ours(a):
             "config": config(a), "clocks": clk,
             "gpu_launches": os2.launch_count(m, n, k, N, a.mode) * a.steps,
             "roofline": roofline, "kernels": kern}
+    if peaks_probe:
+        line["pipe_peaks"] = peaks_probe
 
     # e2e through the host entry point
     if not a.no_e2e:
@@ -502,8 +574,28 @@ def run_ours(a):
         dist.destroy_process_group()
 
 
+def run_peaks_only(a):
+    import torch
+
+    import rns_emulated_fp64_gb300 as os2
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    uuid = str(torch.cuda.get_device_properties(0).uuid)
+    if not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    peaks, src = measured_peaks()
+    out = pipe_peaks(os2, stream, uuid)
+    out["measured_peaks_json"] = {"bf16_tflops": peaks.get("bf16_tflops"),
+                                  "bf16_tflops_sustained": peaks.get("bf16_tflops_sustained"),
+                                  "source": src}
+    print(json.dumps({"pipe_peaks": out}), flush=True)
+
+
 def main():
     a = parse()
+    if a.peaks_only:
+        run_peaks_only(a)
+        return
     if a.impl == "reference":
         run_reference(a)
     else:

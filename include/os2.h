@@ -87,7 +87,9 @@ typedef enum {
  * (N*m*ceil16(n) bytes).  Must be 256-byte aligned. */
 size_t os2_workspace_size(int m, int n, int k, int num_moduli, int mode);
 
-/* The whole five-step emulated DGEMM, C = A*B.  Layouts above.  Returns after
+/* The whole five-step emulated DGEMM, C = A*B ([Q] "行列積への当てはめ方": the
+ * five steps applied to a matrix product; step 1 in fast mode follows [G]
+ * "Methodik").  Layouts above.  Returns after
  * enqueueing on `stream`.  For m >= 4096 the rows of A go in panels of about
  * 2048: the CRT and unscaling of one panel run on a library-owned stream
  * (created once per device, non-blocking) beside the product of the next; that
@@ -160,7 +162,10 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
                      int num_moduli, int mode, int32_t *e, int32_t *f, void *workspace,
                      size_t workspace_bytes, void *stream);
 
-/* Step 2 alone for one operand: rows x k matrix X (row-major, ldx >= k; pass B
+/* Step 2 alone for one operand ([Q] "2の累乗による整数化(手順1と5)": truncation of
+ * the scaled entries to integers; [Q] "256以下の法の選び方(手順2)": their
+ * symmetric residues, for p = 256 the low byte read as int8): rows x k
+ * matrix X (row-major, ldx >= k; pass B
  * as its n columns), exponents exps (rows int32).  Writes N planes of FP16
  * symmetric residues, planes[(l*rows + r)*ldp + h] = sym(trunc(x_rh 2^exps_r) mod p_l),
  * for h < ldp; entries h >= k are written as 0.  ldp >= k, ldp % 64 == 0.
@@ -170,7 +175,9 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
 os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t *exps,
                         int num_moduli, void *planes, int ldp, void *stream);
 
-/* Step 3 alone: N residue matrix products from FP16 planes RA (N x m x ldp)
+/* Step 3 alone ([Q] "誤差のないINT8行列積(手順3)": one exact integer product of
+ * the residue matrices per modulus, reduced mod p_l; larger inner dimensions
+ * split into blocks): N residue matrix products from FP16 planes RA (N x m x ldp)
  * and RB (N x n x ldp), ldp % 64 == 0, k <= ldp.  out_kind selects int8
  * c_l = sym(G_l mod p_l) or raw int32 G_l; out is [N][m][ldo] with ldo >= n
  * (ldo % 16 == 0 for int8, % 4 for int32).  variant: an os2_gemm_variant.
@@ -179,7 +186,11 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
                              int num_moduli, int out_kind, void *out, int ldo, int variant,
                              void *stream);
 
-/* Steps 4 and 5: from c (int8 [N][m][ldcres]) and the exponents, writes
+/* Steps 4 and 5 ([Q] "高い精度での復元(手順4)": reconstruction of the integer
+ * product from its residues beyond double precision; [Q] "繰り上がりのない計算"
+ * and "秦九韶の大衍求一術": X = (sum_l c_l M_l inv_l) mod P; [Q]
+ * "2の累乗による整数化(手順1と5)": the division by mu_i nu_j): from c (int8
+ * [N][m][ldcres]) and the exponents, writes
  * C[i*ldc + j] = RN(X_ij * 2^-(e_i + f_j)) with X the CRT value in
  * [-P/2, P/2).  If X_out is not NULL it also receives X as 8 little-endian
  * 32-bit limbs (two's complement) per entry, X_out[(i*n + j)*8 + u]. */
@@ -190,7 +201,13 @@ os2_status os2_crt(int m, int n, const int8_t *c, int ldcres, int num_moduli, co
 int os2_moduli(int num_moduli, int32_t *out);
 
 /* Synchronises `stream`, returns the device status word of the current
- * device and clears it. */
+ * device and clears it.  The word records errors only the kernels can see:
+ * non-finite inputs ([Q] "行列積の回数と性能" lists Inf/NaN handling among the
+ * points an emulated GEMM must settle; OS II itself gives no rule, so they
+ * are rejected with OS2_ERR_NONFINITE), an out-of-range integer in
+ * os2_residues (OS2_ERR_RANGE) and a device-side wait that timed out
+ * (OS2_ERR_TIMEOUT).  Returns OS2_ERR_CUDA if the synchronisation or the
+ * read fails. */
 os2_status os2_get_status(void *stream);
 
 /* Self-test of the device-side failure detection (the pages have no
@@ -234,6 +251,34 @@ int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode);
 os2_status os2_profile_start(void);
 int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launches);
 
+/* Pipe-peak probes (a measurement aid; the pages have no counterpart): the
+ * throughput ceiling of the tensor-core instructions this library can use on
+ * sm_103a, from its own kernels, as a same-pipe denominator for step 3.
+ *   OS2_PROBE_F16_1SM  tcgen05.mma kind::f16, cta_group::1, 128x256x16 per
+ *                      instruction, one CTA per SM
+ *   OS2_PROBE_F16_2SM  tcgen05.mma kind::f16, cta_group::2, 256x256x16 per
+ *                      instruction, CTA pairs (the form step 3 uses)
+ *   OS2_PROBE_S8_SYNC  mma.sync m16n8k32 s8 x s8 -> s32 (INT8 tensor path
+ *                      outside tcgen05; sm_103a has no tcgen05 kind::i8)
+ * Operands are small integers resident in shared memory (tcgen05) or
+ * registers (mma.sync), so every product is exact.  Enqueues one launch of
+ * `iters` rounds (each round: K = 64 per accumulator tile; for mma.sync eight
+ * independent m16n8k32 per warp) on `stream` and writes to *flop (host, may be
+ * NULL) the flops it performs, counting a multiply-add as 2.  With check != 0
+ * the result is compared with the exact product on the CUDA cores and
+ * result[0] (device int32[4], zeroed by this call) receives the mismatches,
+ * result[1] the number of CTAs that checked; time only runs with check = 0
+ * (result may then be NULL).  iters in [1, 2^24]; check runs of
+ * OS2_PROBE_S8_SYNC need iters <= 4096 (int32 sums).  Bounded waits as in the
+ * GEMM kernels (OS2_ERR_TIMEOUT in the status word on expiry). */
+typedef enum {
+  OS2_PROBE_F16_1SM = 0,
+  OS2_PROBE_F16_2SM = 1,
+  OS2_PROBE_S8_SYNC = 2
+} os2_probe_kind;
+os2_status os2_peak_probe(int kind, int iters, int check, int32_t *result, double *flop,
+                          void *stream);
+
 /* os2_gemm without a caller-supplied workspace, for callers that cannot
  * allocate device memory where they call it: a host library or plugin whose
  * device memory is planned and owned by another allocator (an inference
@@ -248,7 +293,10 @@ int os2_profile_stop(int max_kernels, char *names, double *total_ms, int *launch
  * the process exits.  Problems whose os2_workspace_size exceeds it are
  * rejected with OS2_ERR_WORKSPACE before anything is enqueued (for example
  * m = n = k = 1024 fits for every num_moduli <= 20; at 2048^3 only
- * num_moduli <= 6 fits).
+ * num_moduli <= 6 fits).  With k = 0 it only zeroes C, whatever the sizes.
+ * It runs the five steps in one pass on `stream`, never through os2_gemm's
+ * row-panel pipeline (which creates library streams and events on first
+ * use), so for m >= 4096 it gives the same results a little more slowly.
  * The first call on a device looks up the array's device address with that
  * device current (make that first call before any stream capture); later
  * calls reuse it.  Nothing here calls cudaMalloc, cudaFree or an allocating

@@ -27,7 +27,7 @@ EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gem
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
            "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
            "os2_gemm_noalloc", "os2_sgemm", "os2_complex_workspace_size", "os2_zgemm",
-           "os2_cgemm", "os2_wait_selftest")
+           "os2_cgemm", "os2_wait_selftest", "os2_peak_probe")
 
 _lib = None
 _lock = threading.Lock()
@@ -98,6 +98,8 @@ def load(build_if_missing: bool = True):
         L.os2_wait_selftest.argtypes = [ct.c_longlong, vp, vp]
         L.os2_wait_selftest.restype = i
         L.os2_cgemm.restype = i
+        L.os2_peak_probe.argtypes = [i, i, i, vp, ct.POINTER(ct.c_double), vp]
+        L.os2_peak_probe.restype = i
         _lib = L
         return L
 
@@ -166,6 +168,25 @@ def set_gemm_variant(variant: int):
 
 def get_status(stream=None) -> int:
     return int(load().os2_get_status(_stream(stream)))
+
+
+PROBE_F16_1SM, PROBE_F16_2SM, PROBE_S8_SYNC = 0, 1, 2
+
+
+def peak_probe(kind: int, iters: int, check: bool = False, stream=None):
+    """Enqueue one pipe-peak probe launch (see os2_peak_probe).  Returns the
+    flop it performs; with check=True it synchronises and returns
+    (flop, mismatches, ctas_checked) instead."""
+    fl = ct.c_double(0.0)
+    res = torch.zeros(4, dtype=torch.int32, device="cuda") if check else None
+    _check(load().os2_peak_probe(int(kind), int(iters), 1 if check else 0,
+                                 _ptr(res) if check else None, ct.byref(fl), _stream(stream)),
+           "os2_peak_probe")
+    if not check:
+        return fl.value
+    torch.cuda.synchronize()
+    r = res.cpu().tolist()
+    return fl.value, int(r[0]), int(r[1])
 
 
 def wait_selftest(limit_cycles: int = 2_000_000, stream=None) -> list[int]:

@@ -984,6 +984,24 @@ os2_status os2_get_status(void *stream) {
   return static_cast<os2_status>(v);
 }
 
+os2_status os2_peak_probe(int kind, int iters, int check, int32_t *result, double *flop,
+                          void *stream) {
+  if (kind != OS2_PROBE_F16_1SM && kind != OS2_PROBE_F16_2SM && kind != OS2_PROBE_S8_SYNC)
+    return OS2_ERR_INVALID_ARG;
+  if (iters < 1 || iters > (1 << 24)) return OS2_ERR_INVALID_ARG;
+  if (check && (!result || !aligned(result, 4))) return OS2_ERR_INVALID_ARG;
+  if (check && kind == OS2_PROBE_S8_SYNC && iters > 4096) return OS2_ERR_INVALID_ARG;
+  int *status = os2_status_ptr();
+  if (!status) return OS2_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (check && (err = cudaMemsetAsync(result, 0, 4 * sizeof(int32_t), s))) return cuda_status(err);
+  double fl = 0;
+  err = launch_peak_probe(kind, iters, check ? 1 : 0, result, status, s, &fl);
+  if (flop) *flop = fl;
+  return cuda_status(err);
+}
+
 os2_status os2_set_gemm_variant(int variant) {
   if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM)
     return OS2_ERR_INVALID_ARG;
@@ -1103,9 +1121,13 @@ extern "C" os2_status os2_gemm_noalloc(int m, int n, int k, const double *A, int
   Layout L;
   make_layout(m, n, k, num_moduli, mode, &L);
   if (m == 0 || n == 0) return OS2_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // k == 0: C = 0 and no scratch is touched, whatever the sizes (as os2_gemm)
+  if (k == 0) return run_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, nullptr, L, s);
   if (L.total > (size_t)OS2_NOALLOC_SCRATCH_BYTES) return OS2_ERR_WORKSPACE;
   void *ws = noalloc_scratch();
   if (!ws) return OS2_ERR_CUDA;
-  return run_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, ws, L,
-                  static_cast<cudaStream_t>(stream));
+  // one pass on the caller's stream: the row-panel pipeline of os2_gemm would
+  // create library streams and events on first use
+  return run_gemm(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, mode, ws, L, s);
 }

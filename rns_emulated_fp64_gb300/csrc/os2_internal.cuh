@@ -69,6 +69,10 @@ int *os2_status_ptr();
 // One CTA whose bounded mbarrier waits run out (failure-detection self-test).
 cudaError_t launch_wait_selftest(long long limit, int *status, int32_t *result, cudaStream_t s);
 
+// Pipe-peak probes (os2_peak_probe).  Writes the flop one launch does to *flop.
+cudaError_t launch_peak_probe(int kind, int iters, int check, int32_t *result, int *status,
+                              cudaStream_t s, double *flop);
+
 // Row-scale kernel modes.
 enum ScaleMode {
   SM_FAST_SCALE = 0,   // fast mode: e_i from the revised bound

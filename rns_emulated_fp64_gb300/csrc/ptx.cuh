@@ -1,5 +1,8 @@
 // Inline-PTX wrappers for sm_103a: mbarrier, TMA (cp.async.bulk.tensor),
-// tcgen05 (TMEM allocation, MMA, commit, loads/stores).  No multicast.
+// tcgen05 (TMEM allocation, MMA, commit, loads/stores).  No multicast loads:
+// every TMA copy lands in the issuing CTA's own shared memory; the only
+// multicast is the 2-SM MMA commit, which signals the mbarriers of both CTAs
+// of a pair.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>

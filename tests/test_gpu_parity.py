@@ -408,6 +408,26 @@ def test_host_entry_point_matches_device(mode, m, n, k, pinned):
     assert_bits_equal(Ch.numpy(), Cd, "host vs device entry")
 
 
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+def test_host_entry_point_oracle_sample(mode):
+    """The host entry point checked against the oracle directly (not only
+    against os2_gemm): several row and column panels, ragged edges, a seeded
+    48 x 48 sample with the last row and column."""
+    m, n, k = 4700, 4400, 200
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=31, phi=2.0)
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(Bt).pin_memory()
+    Ch = torch.full((m, n), np.nan, dtype=torch.float64).pin_memory()
+    os2.gemm_host(Ah, Bh, Ch, 16, mode)
+    torch.cuda.current_stream().synchronize()
+    status_ok()
+    rows, cols = workloads.sample_grid(m, n, 48, seed=7)
+    ref = orc.gemm_entries(A, Bt, 16, rows, cols, mode=orc.FAST if mode == "fast" else orc.ACCURATE,
+                           want_X=False, want_c=False, want_G=False)
+    assert ref.mismatches == 0
+    assert_bits_equal(Ch.numpy()[np.ix_(rows, cols)], ref.C, f"host entry point {mode}")
+
+
 def test_host_entry_point_strided_back_to_back():
     """Row strides on all three host matrices, a side stream, and two calls in
     a row on one workspace with one synchronisation at the end: the second
