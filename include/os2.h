@@ -77,6 +77,11 @@ typedef enum {
 } os2_gemm_variant;
 
 typedef enum {
+  OS2_CRT_TC = 0,         /* limb sums as an FP16 tensor-core MMA per 128 entries (default) */
+  OS2_CRT_SIMT = 1        /* limb sums as 32x32->64 multiply-adds on the CUDA cores */
+} os2_crt_variant;
+
+typedef enum {
   OS2_OUT_MODP_INT8 = 0,  /* c_l = G_l mod p_l, symmetric, int8 [N][m][ldo] */
   OS2_OUT_RAW_INT32 = 1   /* G_l itself, int32 [N][m][ldo] */
 } os2_out_kind;
@@ -90,13 +95,15 @@ size_t os2_workspace_size(int m, int n, int k, int num_moduli, int mode);
 /* The whole five-step emulated DGEMM, C = A*B ([Q] "行列積への当てはめ方": the
  * five steps applied to a matrix product; step 1 in fast mode follows [G]
  * "Methodik").  Layouts above.  Returns after
- * enqueueing on `stream`.  For m >= 4096 the rows of A go in panels of about
- * 2048: the CRT and unscaling of one panel run on a library-owned stream
- * (created once per device, non-blocking) beside the product of the next; that
- * stream first waits for the work already on `stream`, and `stream` waits for
- * it before the call's work ends, so synchronising `stream` covers the call.
- * Results are identical either way.  Calls from several host threads are
- * enqueued one at a time. */
+ * enqueueing on `stream`.  With the default reconstruction kernel
+ * (OS2_CRT_TC) every step runs on `stream`, once over the whole problem.
+ * With OS2_CRT_SIMT (os2_set_crt_variant) and m >= 4096 the rows of A go in
+ * panels of about 2048: the CRT and unscaling of one panel run on a
+ * library-owned stream (created once per device, non-blocking) beside the
+ * product of the next; that stream first waits for the work already on
+ * `stream`, and `stream` waits for it before the call's work ends, so
+ * synchronising `stream` covers the call.  Results are identical either way.
+ * Calls from several host threads are enqueued one at a time. */
 os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
                     double *C, int ldc, int num_moduli, int mode, void *workspace,
                     size_t workspace_bytes, void *stream);
@@ -225,6 +232,17 @@ os2_status os2_get_status(void *stream);
  * wait lasted at least limit_cycles; [5..7] 0.  Returns OS2_ERR_INVALID_ARG
  * for a limit out of range (nothing enqueued). */
 os2_status os2_wait_selftest(long long limit_cycles, int32_t *result, void *stream);
+
+/* Selects the kernel of steps 4 and 5 (process-wide; default OS2_CRT_TC).
+ * Both give bit-identical results.  OS2_CRT_TC computes the sums
+ * sum_l (c_l + 128) W_l as an FP16 tensor-core product of the residues with
+ * the signed 10-bit digits of the W_l, exact in FP32; it needs rows of c that
+ * are 16-byte aligned (os2_crt falls back to OS2_CRT_SIMT otherwise).  With
+ * OS2_CRT_TC, os2_gemm runs in one pass (one product launch); with
+ * OS2_CRT_SIMT it cuts A into row panels for m >= 4096 and runs each panel's
+ * reconstruction on the CUDA cores beside the next panel's product.
+ * OS2_ERR_INVALID_ARG for another value. */
+os2_status os2_set_crt_variant(int variant);
 
 /* Selects the step-3 kernel used by os2_gemm (process-wide; default TC). */
 os2_status os2_set_gemm_variant(int variant);

@@ -9,4 +9,5 @@ from .binding import (GEMM_SIMT, GEMM_TC, GEMM_TC_1SM, MODE_ACCURATE, MODE_FAST,
                       matmul, moduli, profile_start, profile_stop, residues, scale, sgemm,
                       set_gemm_variant, status_string, workspace_size, zgemm,
                       complex_workspace_size, wait_selftest, ERR_TIMEOUT, peak_probe,
-                      PROBE_F16_1SM, PROBE_F16_2SM, PROBE_S8_SYNC)
+                      PROBE_F16_1SM, PROBE_F16_2SM, PROBE_S8_SYNC, set_crt_variant,
+                      CRT_TC, CRT_SIMT)

@@ -18,6 +18,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, 1, 2, 3
 ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA = 4, 5, 6, 7
 MODE_FAST, MODE_ACCURATE = 0, 1
 GEMM_TC, GEMM_SIMT, GEMM_TC_1SM = 0, 1, 2
+CRT_TC, CRT_SIMT = 0, 1
 OUT_MODP_INT8, OUT_RAW_INT32 = 0, 1
 KP_ALIGN, CRES_ALIGN = 64, 16
 
@@ -27,7 +28,7 @@ EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gem
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
            "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
            "os2_gemm_noalloc", "os2_sgemm", "os2_complex_workspace_size", "os2_zgemm",
-           "os2_cgemm", "os2_wait_selftest", "os2_peak_probe")
+           "os2_cgemm", "os2_wait_selftest", "os2_peak_probe", "os2_set_crt_variant")
 
 _lib = None
 _lock = threading.Lock()
@@ -100,6 +101,8 @@ def load(build_if_missing: bool = True):
         L.os2_cgemm.restype = i
         L.os2_peak_probe.argtypes = [i, i, i, vp, ct.POINTER(ct.c_double), vp]
         L.os2_peak_probe.restype = i
+        L.os2_set_crt_variant.argtypes = [i]
+        L.os2_set_crt_variant.restype = i
         _lib = L
         return L
 
@@ -164,6 +167,12 @@ def launch_count(m, n, k, num_moduli, mode="fast") -> int:
 
 def set_gemm_variant(variant: int):
     _check(load().os2_set_gemm_variant(int(variant)), "os2_set_gemm_variant")
+
+
+def set_crt_variant(variant: int):
+    """Kernel of steps 4 + 5: CRT_TC (tensor-core limb sums, default) or
+    CRT_SIMT (CUDA-core multiply-adds); results are bit-identical."""
+    _check(load().os2_set_crt_variant(int(variant)), "os2_set_crt_variant")
 
 
 def get_status(stream=None) -> int:

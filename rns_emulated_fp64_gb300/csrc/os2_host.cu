@@ -70,6 +70,16 @@ U256 u_div(const U256 &a, uint32_t d, uint32_t *rem) {
   if (rem) *rem = (uint32_t)r;
   return q;
 }
+U256 u_sub_small(const U256 &a, uint32_t v) {
+  U256 r = a;
+  uint64_t b = v;
+  for (int i = 0; i < 8 && b; i++) {
+    const uint64_t cur = r.w[i];
+    r.w[i] = (uint32_t)(cur - b);
+    b = cur < b ? 1 : 0;
+  }
+  return r;
+}
 U256 u_sub1(const U256 &a) {
   U256 r = a;
   for (int i = 0; i < 8; i++) {
@@ -81,6 +91,51 @@ U256 u_shr1(const U256 &a) {
   U256 r;
   for (int i = 0; i < 8; i++) r.w[i] = (a.w[i] >> 1) | (i + 1 < 8 ? a.w[i + 1] << 31 : 0u);
   return r;
+}
+U256 u_add(const U256 &a, const U256 &b) {
+  U256 r;
+  uint64_t c = 0;
+  for (int i = 0; i < 8; i++) {
+    c += (uint64_t)a.w[i] + b.w[i];
+    r.w[i] = (uint32_t)c;
+    c >>= 32;
+  }
+  return r;
+}
+U256 u_neg(const U256 &a) {  // two's complement modulo 2^256
+  U256 r;
+  uint64_t c = 1;
+  for (int i = 0; i < 8; i++) {
+    c += (uint64_t)(~a.w[i]);
+    r.w[i] = (uint32_t)c;
+    c >>= 32;
+  }
+  return r;
+}
+U256 u_shl(const U256 &a, int s) {
+  U256 r = {};
+  for (int i = 7; i >= 0; i--) {
+    const int src = i - s / 32, o = s % 32;
+    uint32_t v = src >= 0 ? a.w[src] << o : 0u;
+    if (o && src - 1 >= 0) v |= a.w[src - 1] >> (32 - o);
+    r.w[i] = v;
+  }
+  return r;
+}
+U256 u_shr(const U256 &a, int s) {
+  U256 r = {};
+  for (int i = 0; i < 8; i++) {
+    const int src = i + s / 32, o = s % 32;
+    uint32_t v = src < 8 ? a.w[src] >> o : 0u;
+    if (o && src + 1 < 8) v |= a.w[src + 1] << (32 - o);
+    r.w[i] = v;
+  }
+  return r;
+}
+bool u_zero(const U256 &a) {
+  for (int i = 0; i < 8; i++)
+    if (a.w[i]) return false;
+  return true;
 }
 int u_bitlen(const U256 &a) {
   for (int i = 7; i >= 0; i--)
@@ -157,6 +212,57 @@ void build_tables(int N, Os2Tables *t) {
     t->crt.P32[v] = P.w[v];
     t->crt.H32[v] = half.w[v];
   }
+  // Tensor-core CRT: signed 10-bit digits of the W_l, W_l = sum_t w_{l,t} 2^(10 t)
+  {
+    CrtTcConsts &k = t->crt_tc;
+    k.N = N;
+    k.LX = 1;  // smallest limb count with 2^(32 LX) > 3P
+    {
+      const U256 P3 = u_mul(P, 3);
+      while (k.LX < 8 && u_bitlen(P3) > 32 * k.LX) k.LX++;
+    }
+    int T = 0;
+    for (int l = 0; l < N; l++) {
+      const U256 M = u_div(P, (uint32_t)kModuli[l], nullptr);
+      U256 W = u_mul(M, (uint32_t)t->inv[l]);
+      int d = 0;
+      while (!u_zero(W)) {
+        int r = (int)(W.w[0] & 1023u);
+        if (r >= 512) r -= 1024;
+        if (d < OS2_CRT_DIGITS) k.wd[l][d] = (int16_t)r;
+        // (W - r) / 2^10: exact, W - r >= 0
+        W = r >= 0 ? u_shr(u_sub_small(W, (uint32_t)r), 10) : u_shr(u_add(W, u_from((uint32_t)-r)), 10);
+        d++;
+      }
+      T = std::max(T, d);
+    }
+    k.T = std::min(T, OS2_CRT_DIGITS + 1);  // > OS2_CRT_DIGITS is rejected at launch
+    const int LX = k.LX;
+    const double Pd = u_to_double(P);
+    for (int q = 1; q <= T; q++) {  // top digits that fix q to within 2^-11
+      k.Q = q;
+      if (255.0 * 512.0 * N * ldexp(1.0, 10 * (T - q)) * 1.001 / Pd <= ldexp(1.0, -11)) break;
+    }
+    U256 C0 = {};
+    for (int tt = 0; tt < T && tt < OS2_CRT_DIGITS; tt++) {
+      long long sumw = 0;
+      for (int l = 0; l < N; l++) sumw += k.wd[l][tt];
+      k.rmag[tt] = 12582912.0f - 1024.0f * (float)sumw;  // exact: a multiple of 1024 below 2^25
+      k.pw[tt] = 1u << ((10 * tt) & 31);
+      if (10 * tt < 32 * LX) C0 = u_add(C0, u_shl(u_from(0x4B400000u), 10 * tt));
+    }
+    const U256 negc = u_neg(u_add(C0, u_from(128)));
+    const U256 np = u_neg(P);
+    for (int v = 0; v < 5; v++) {
+      k.negc[v] = v < LX ? negc.w[v] : 0;
+      k.np[v] = v < LX ? np.w[v] : 0;
+      k.P32[v] = P.w[v];
+      k.H32[v] = half.w[v];
+    }
+    for (int j = 0; j < k.Q && j < OS2_CRT_DIGITS; j++)
+      k.s[j] = (float)(ldexp(1.0, 10 * (T - 1 - j)) / Pd);
+    k.c0 = (float)(-128.0 / Pd);
+  }
   const int LW = (N + 3) / 4;
   const double Pd = u_to_double(P);
   t->crt.s_top = (float)(ldexp(1.0, 32 * (LW - 1)) / Pd);
@@ -177,6 +283,7 @@ void build_tables(int N, Os2Tables *t) {
 }
 
 std::atomic<int> g_variant{OS2_GEMM_TC};
+std::atomic<int> g_crt_variant{OS2_CRT_TC};
 
 // Optional per-kernel timing: CUDA events recorded on the launching stream
 // around every kernel that os2_gemm enqueues (no synchronisation added).
@@ -265,6 +372,20 @@ bool make_layout(int m, int n, int k, int N, int mode, Layout *L) {
 }
 
 os2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OS2_OK : OS2_ERR_CUDA; }
+
+// Steps 4 + 5 on the selected kernel: the tensor-core one needs 16-byte rows
+// of the product residues (always so inside the library).
+bool crt_on_tc(int ldcres, const void *c) {
+  return g_crt_variant.load() == OS2_CRT_TC && ldcres % 16 == 0 &&
+         (reinterpret_cast<uintptr_t>(c) & 15) == 0;
+}
+cudaError_t crt_launch(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
+                       const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
+                       int *status, cudaStream_t s) {
+  if (crt_on_tc(ldcres, c))
+    return launch_crt_tc(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, status, s);
+  return launch_crt(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, s);
+}
 
 template <typename T>
 T *at(void *ws, size_t off) {
@@ -401,7 +522,7 @@ os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const
   if (st) return st;
   // steps 4 + 5
   ProfScope ps("crt_unscale", s);
-  return cuda_status(launch_crt(f32, m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, s));
+  return cuda_status(crt_launch(f32, m, n, cres, L.ldcres, e, f, C, ldc, nullptr, t, status, s));
 }
 
 // Device-path pipeline.  Step 3 fills every SM with one persistent CTA that
@@ -491,8 +612,8 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
     OS2_TRY(cudaEventRecord(p->g_done[i], s));
     OS2_TRY(cudaStreamWaitEvent(p->crt, p->g_done[i], 0));
     ProfScope ps("crt_unscale", p->crt);
-    OS2_TRY(launch_crt(f32, mi, n, ci, L.ldcres, e + r0, f, Cb + (size_t)r0 * ldc * es, ldc,
-                       nullptr, t, p->crt));
+    OS2_TRY(crt_launch(f32, mi, n, ci, L.ldcres, e + r0, f, Cb + (size_t)r0 * ldc * es, ldc,
+                       nullptr, t, status, p->crt));
   }
   // `stream` covers everything: it waits for the last reconstruction
   OS2_TRY(cudaEventRecord(p->done, p->crt));
@@ -501,11 +622,17 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
   return OS2_OK;
 }
 
+// Row panels pay only with the CUDA-core CRT, which runs on the units the
+// product leaves idle.  The tensor-core CRT needs TMEM and more shared memory
+// than a product CTA leaves free, so it cannot run beside a product: with it
+// the five steps run in one pass (one product launch, no panel tails).
+bool use_panels(int m) { return panel_size(m) < m && g_crt_variant.load() != OS2_CRT_TC; }
+
 // run_gemm_panels when A has more than one row panel, else run_gemm.
 os2_status run_gemm_auto(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
                          int ldb, void *C, int ldc, int N, int mode, void *ws, const Layout &L,
                          cudaStream_t s) {
-  if (m > 0 && n > 0 && k > 0 && panel_size(m) < m)
+  if (m > 0 && n > 0 && k > 0 && use_panels(m))
     return run_gemm_panels(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s);
   return run_gemm(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s);
 }
@@ -817,18 +944,23 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
                              L.ldcres, nullptr, nullptr, 14, t, status, s, n);
       if (err) return cuda_status(err);
     }
-    // the block's CRT runs on the CRT stream beside the next block's product
+    // the block's CRT: the CUDA-core kernel runs on the CRT stream beside the
+    // next block's product; the tensor-core one follows the product on `stream`
     cudaEvent_t gd = p->g_done[blocks], done = p->c_done[blocks];
     blocks++;
-    if ((err = cudaEventRecord(gd, s))) return cuda_status(err);
-    if ((err = cudaStreamWaitEvent(p->crt, gd, 0))) return cuda_status(err);
+    const bool tc = crt_on_tc(L.ldcres, ci);
+    cudaStream_t cs = tc ? s : p->crt;
+    if (!tc) {
+      if ((err = cudaEventRecord(gd, s))) return cuda_status(err);
+      if ((err = cudaStreamWaitEvent(p->crt, gd, 0))) return cuda_status(err);
+    }
     {
-      ProfScope ps("crt_unscale", p->crt);
-      if ((err = launch_crt(false, mi, nj, ci, L.ldcres, e + r0, f + c0,
-                            dC + (size_t)r0 * n + c0, n, nullptr, t, p->crt)))
+      ProfScope ps("crt_unscale", cs);
+      if ((err = crt_launch(false, mi, nj, ci, L.ldcres, e + r0, f + c0, dC + (size_t)r0 * n + c0,
+                            n, nullptr, t, status, cs)))
         return cuda_status(err);
     }
-    if ((err = cudaEventRecord(done, p->crt))) return cuda_status(err);
+    if ((err = cudaEventRecord(done, cs))) return cuda_status(err);
     if ((err = cudaStreamWaitEvent(p->out, done, 0))) return cuda_status(err);
     return cuda_status(copy_rows(C + (size_t)r0 * ldc + c0, ldc, dC + (size_t)r0 * n + c0, n, nj,
                                  mi, cudaMemcpyDeviceToHost, p->out));
@@ -954,8 +1086,9 @@ os2_status os2_crt(int m, int n, const int8_t *c, int ldcres, int num_moduli, co
   if (m == 0 || n == 0) return OS2_OK;
   if (!c || !e || !f || !C || !aligned(c, 4) || !aligned(C, 8)) return OS2_ERR_INVALID_ARG;
   const Os2Tables *t = os2_tables(num_moduli);
-  if (!t) return OS2_ERR_CUDA;
-  return cuda_status(launch_crt(false, m, n, c, ldcres, e, f, C, ldc, X_out, t,
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  return cuda_status(crt_launch(false, m, n, c, ldcres, e, f, C, ldc, X_out, t, status,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -1000,6 +1133,12 @@ os2_status os2_peak_probe(int kind, int iters, int check, int32_t *result, doubl
   err = launch_peak_probe(kind, iters, check ? 1 : 0, result, status, s, &fl);
   if (flop) *flop = fl;
   return cuda_status(err);
+}
+
+os2_status os2_set_crt_variant(int variant) {
+  if (variant != OS2_CRT_TC && variant != OS2_CRT_SIMT) return OS2_ERR_INVALID_ARG;
+  g_crt_variant.store(variant);
+  return OS2_OK;
 }
 
 os2_status os2_set_gemm_variant(int variant) {
@@ -1076,7 +1215,7 @@ int os2_gemm_launch_count(int m, int n, int k, int num_moduli, int mode) {
   if (k == 0) return 0;
   // os2_gemm: step 1 (fast: 1 kernel; accurate: bars, the bound product,
   // two exponent kernels), then residues, product and CRT once per row panel
-  const int mp = panel_size(m), P = mp < m ? (m + mp - 1) / mp : 1;
+  const int P = use_panels(m) ? (m + panel_size(m) - 1) / panel_size(m) : 1;
   if (mode != OS2_MODE_ACCURATE) return 1 + 3 * P;
   Layout L;
   if (!make_layout(m, n, k, num_moduli, mode, &L)) return 0;

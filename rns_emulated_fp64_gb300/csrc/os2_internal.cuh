@@ -42,6 +42,23 @@ struct CrtConsts {
   float s128;                        // fl(128 / P)
 };
 
+// Steps 4-5 on the tensor cores (k_crt_tc): W_l in signed 10-bit digits,
+// W_l = sum_t w_{l,t} 2^(10 t), |w| <= 512; the digit sums of Y = sum_l (c_l +
+// 128) W_l come out of one FP16 MMA per 128 entries.
+#define OS2_CRT_DIGITS 16
+struct CrtTcConsts {
+  int N, T, LX, Q;                                // moduli, digits, 32-bit limbs of X, digits for q
+  int16_t wd[OS2_MAX_MODULI][OS2_CRT_DIGITS];     // w_{l,t}
+  float rmag[OS2_CRT_DIGITS];                     // 1.5 * 2^23 - 1024 sum_l w_{l,t}
+  uint32_t pw[OS2_CRT_DIGITS];                    // 2^(10 t mod 32)
+  uint32_t negc[5];                               // -(C0 + 128) mod 2^(32 LX)
+  uint32_t np[5];                                 // 2^(32 LX) - P
+  uint32_t P32[5];                                // P
+  uint32_t H32[5];                                // P / 2
+  float s[OS2_CRT_DIGITS];                        // 2^(10 (T - 1 - j)) / P, j < Q
+  float c0;                                       // -128 / P
+};
+
 // Step-3 constants.
 struct GemmConsts {
   int N;
@@ -57,6 +74,7 @@ struct Os2Tables {
   int32_t inv[OS2_MAX_MODULI];
   ResConsts res;
   CrtConsts crt;
+  CrtTcConsts crt_tc;
   GemmConsts gemm;
 };
 
@@ -96,6 +114,11 @@ cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int ro
 cudaError_t launch_crt(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
                        const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
                        cudaStream_t s);
+// Steps 4 + 5 on the tensor cores; needs ldcres % 16 == 0 and a 16-byte
+// aligned c (else cudaErrorInvalidValue).
+cudaError_t launch_crt_tc(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
+                          const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
+                          int *status, cudaStream_t s);
 cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *RB, int N,
                              int out_kind, void *out, int ldo, const Os2Tables *t, cudaStream_t s);
 

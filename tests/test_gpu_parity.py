@@ -38,6 +38,15 @@ def check_tolerance(C, A, Bt, rows, cols, ref):
     assert np.all(np.abs(C - ref) <= TOL * absprod)
 
 
+@pytest.fixture(params=[os2.CRT_TC, os2.CRT_SIMT], ids=["crt_tc", "crt_simt"])
+def crt_variant(request):
+    """Runs a test with each kernel of steps 4 + 5 (tensor-core limb sums and
+    CUDA-core multiply-adds); both must give the oracle's bits."""
+    os2.set_crt_variant(request.param)
+    yield request.param
+    os2.set_crt_variant(os2.CRT_TC)
+
+
 SHAPES = [(64, 64, 64), (1, 1, 1), (3, 5, 7), (129, 257, 65), (300, 520, 1000), (128, 256, 960),
           (130, 140, 1921)]
 
@@ -196,7 +205,7 @@ def test_modp_alternating_extremes():
 
 # --------------------------------------------------------------- steps 4-5 --
 @pytest.mark.parametrize("N", [1, 2, 4, 5, 8, 9, 12, 13, 14, 16, 17, 20])
-def test_crt_parity_from_oracle_residues(N):
+def test_crt_parity_from_oracle_residues(N, crt_variant):
     A, Bt = workloads.make_pair("spread", 37, 45, 90, seed=N, phi=2.0)
     ref = orc.gemm_entries(A, Bt, N)
     cres = np.zeros((N, 37, 48), np.int8)
@@ -207,8 +216,26 @@ def test_crt_parity_from_oracle_residues(N):
     assert_bits_equal(C.cpu().numpy(), ref.C, "C")
 
 
+@pytest.mark.parametrize("ldcres", [48, 52, 45])
+def test_crt_unaligned_rows_fall_back(ldcres):
+    """Rows of c that are not 16-byte multiples take the CUDA-core kernel
+    (the tensor-core one reads 16-byte vectors): same bits."""
+    N, m, n = 16, 21, 45
+    A, Bt = workloads.make_pair("spread", m, n, 70, seed=ldcres, phi=2.0)
+    ref = orc.gemm_entries(A, Bt, N)
+    cres = np.zeros((N, m, ldcres), np.int8)
+    cres[:, :, :n] = np.transpose(ref.c, (2, 0, 1))
+    if ldcres % 4:
+        with pytest.raises(os2.Os2Error):
+            os2.crt(dev(cres), n, dev(ref.e), dev(ref.f))
+        return
+    C = os2.crt(dev(cres), n, dev(ref.e), dev(ref.f))
+    status_ok()
+    assert_bits_equal(C.cpu().numpy(), ref.C, f"ldcres={ldcres}")
+
+
 @pytest.mark.parametrize("N", [1, 2])
-def test_crt_exhaustive_small_moduli_sets(N):
+def test_crt_exhaustive_small_moduli_sets(N, crt_variant):
     """Every residue vector for N = 1 (256 values) and N = 2 (256 x 255):
     X is the unique value in [-P/2, P/2) with those residues (brute force),
     including X = -P/2 itself; with e = f = 0 the result is X exactly."""
@@ -229,7 +256,7 @@ def test_crt_exhaustive_small_moduli_sets(N):
     assert np.array_equal(C.cpu().numpy().reshape(-1), expect)
 
 
-def test_crt_random_residues_and_rounding():
+def test_crt_random_residues_and_rounding(crt_variant):
     """Arbitrary residue vectors (X anywhere in [-P/2, P/2)) and exponents that
     push the result into the subnormal and overflow ranges."""
     rng = np.random.default_rng(2)
@@ -264,7 +291,7 @@ def test_crt_random_residues_and_rounding():
 # ------------------------------------------------------------- end to end --
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
 @pytest.mark.parametrize("m,n,k", SHAPES)
-def test_gemm_end_to_end_small(mode, m, n, k):
+def test_gemm_end_to_end_small(mode, m, n, k, crt_variant):
     N = 14
     A, Bt = workloads.make_pair("spread", m, n, k, seed=k, phi=1.0)
     C = os2.gemm(dev(A), dev(Bt), N, mode).cpu().numpy()
@@ -409,7 +436,7 @@ def test_host_entry_point_matches_device(mode, m, n, k, pinned):
 
 
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
-def test_host_entry_point_oracle_sample(mode):
+def test_host_entry_point_oracle_sample(mode, crt_variant):
     """The host entry point checked against the oracle directly (not only
     against os2_gemm): several row and column panels, ragged edges, a seeded
     48 x 48 sample with the last row and column."""
@@ -607,7 +634,7 @@ def test_row_panels_equal_unpanelled_rows():
 
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
 @pytest.mark.parametrize("m", [4100, 9000])
-def test_row_panels_oracle_sample(mode, m):
+def test_row_panels_oracle_sample(mode, m, crt_variant):
     """Ragged last panel (4100 = 2304 + 1796; 9000 = 3 x 2304 + 2088), both
     modes, a seeded 40 x 40 sample (always with the last row and column)
     bit-exact against the oracle."""
@@ -666,7 +693,7 @@ def test_accurate_bound_segments(N, k):
 
 
 @pytest.mark.parametrize("m,n,k", [(70000, 20, 40), (3, 70000, 40)])
-def test_tall_and_wide_shapes(m, n, k):
+def test_tall_and_wide_shapes(m, n, k, crt_variant):
     """More than 65535 rows of A or columns of B: the residue and CRT grids cap
     their y dimension and loop, and m = 70000 runs the most row panels (8)."""
     A, Bt = workloads.make_pair("spread", m, n, k, seed=m + n, phi=1.0)
