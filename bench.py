@@ -61,6 +61,8 @@ def parse():
                     help="skip the N in {14,16,18} x {fast, accurate} sweep of the same workload")
     ap.add_argument("--no-peaks", action="store_true",
                     help="skip the tensor-pipe peak probes (own kernels) before the timed steps")
+    ap.add_argument("--crt", default="default", choices=["default", "tc", "simt"],
+                    help="kernel of steps 4 + 5 (os2_set_crt_variant); default: the library's")
     ap.add_argument("--peaks-only", action="store_true",
                     help="run only the tensor-pipe peak probes and print them as one JSON line")
     return ap.parse_args()
@@ -325,6 +327,8 @@ def run_ours(a):
     import rns_emulated_fp64_gb300 as os2
     world, rank, local = dist_setup(a)
     dev = torch.device("cuda", local if world > 1 else 0)
+    if a.crt != "default":
+        os2.set_crt_variant(os2.CRT_TC if a.crt == "tc" else os2.CRT_SIMT)
     m, n, k, N = a.m, a.n, a.k, a.num_moduli
     A, Bt = workloads.make_pair("spread", m, n, k, seed=rank, phi=a.phi)
     Ad = torch.from_numpy(A).to(dev)
@@ -425,7 +429,7 @@ def run_ours(a):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config(a), "clocks": clk,
+            "config": config(a, {"crt_kernel": a.crt}), "clocks": clk,
             "gpu_launches": os2.launch_count(m, n, k, N, a.mode) * a.steps,
             "roofline": roofline, "kernels": kern}
     if peaks_probe:

@@ -13,6 +13,14 @@ struct Fmt;
 template <>
 struct Fmt<double> {
   static constexpr int prec = 53, emin = -1022, emax = 1023;
+  // normal number from a significand with its leading bit at bit prec - 1 (or
+  // 2^prec after a rounding carry) and the exponent of that leading bit: the
+  // add carries a full significand into the exponent, up to +-Inf
+  static __device__ __forceinline__ double pack_normal(uint64_t sig, int ex, bool neg) {
+    uint64_t b = ((uint64_t)(ex + 1022) << 52) + sig;
+    if (neg) b |= 1ull << 63;
+    return __longlong_as_double((long long)b);
+  }
   static __device__ __forceinline__ double make(uint64_t mant, int ex, bool neg, int kind) {
     // kind 0: normal (mant has prec bits, ex unbiased); 1: subnormal bits in mant; 2: inf
     uint64_t b = kind == 2 ? 0x7FF0000000000000ull
@@ -24,6 +32,11 @@ struct Fmt<double> {
 template <>
 struct Fmt<float> {
   static constexpr int prec = 24, emin = -126, emax = 127;
+  static __device__ __forceinline__ float pack_normal(uint64_t sig, int ex, bool neg) {
+    uint32_t b = ((uint32_t)(ex + 126) << 23) + (uint32_t)sig;
+    if (neg) b |= 1u << 31;
+    return __uint_as_float(b);
+  }
   static __device__ __forceinline__ float make(uint64_t mant, int ex, bool neg, int kind) {
     uint32_t b = kind == 2 ? 0x7F800000u
                            : (kind == 1 ? (uint32_t)mant
@@ -36,8 +49,17 @@ struct Fmt<float> {
 // RN-even of |X| * 2^-s to the format of OutT, |X| in 32-bit limbs m[0..L),
 // sign `neg` (general routine: zero, subnormal and overflowing results; kept
 // out of line).
+// The limbs are passed as scalars (at most 6): an out-of-line call taking an
+// array (or a struct) made every caller spill its limbs to the stack on every
+// entry, slow path or not.
 template <typename OutT, int L>
-__device__ __noinline__ OutT round_scaled(const uint32_t (&m)[L], bool neg, int s) {
+__device__ __noinline__ OutT round_scaled_v(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3,
+                                            uint32_t m4, uint32_t m5, bool neg, int s) {
+  static_assert(L >= 1 && L <= 6, "at most 6 limbs");
+  const uint32_t all[6] = {m0, m1, m2, m3, m4, m5};
+  uint32_t m[L];
+#pragma unroll
+  for (int u = 0; u < L; u++) m[u] = all[u];
   using F = Fmt<OutT>;
   constexpr int lsb = F::prec - 1 - F::emin;  // -log2 of the smallest subnormal
   int top = -1;
@@ -94,6 +116,12 @@ __device__ __noinline__ OutT round_scaled(const uint32_t (&m)[L], bool neg, int 
   return F::make(kept << (x + lsb), 0, neg, 1);  // subnormal: x >= -lsb by construction of cut
 }
 
+template <typename OutT, int L>
+__device__ __forceinline__ OutT round_scaled(const uint32_t (&m)[L], bool neg, int s) {
+  auto w = [&](int u) { return u < L ? m[u < L ? u : 0] : 0u; };
+  return round_scaled_v<OutT, L>(w(0), w(1), w(2), w(3), w(4), w(5), neg, s);
+}
+
 // Normal-range fast path: the top three nonzero-anchored limbs hold at least
 // 65 significant bits, enough for the significand, the round bit and a sticky
 // bit (OR-ed with everything below).  Falls back to the general routine for
@@ -133,6 +161,30 @@ __device__ __forceinline__ OutT round_scaled_fast(const uint32_t (&m)[L], bool n
     }
   }
   return ex > F::emax ? F::make(0, 0, neg, 2) : F::make(kept, ex, neg, 0);
+}
+
+// RN-even of |X| 2^-s for |X| whose top limb m[L-1] is nonzero and whose
+// result is a normal number (the common case); anything else goes to the
+// general routine.  The significand is the top 64 bits below the leading one
+// of the top limb; the bits below that window only feed the sticky bit.
+template <typename OutT, int L>
+__device__ __forceinline__ OutT round_scaled_top(const uint32_t (&m)[L], bool neg, int s) {
+  using F = Fmt<OutT>;
+  const uint32_t hi = m[L - 1];
+  const int lz = __clz(hi);
+  const int etop = 32 * (L - 1) + 31 - lz - s;  // exponent of the leading bit of |X| 2^-s
+  if (hi == 0 || etop < F::emin || etop > F::emax) return round_scaled<OutT, L>(m, neg, s);
+  const uint32_t mid = L >= 2 ? m[L >= 2 ? L - 2 : 0] : 0u;
+  const uint32_t lo = L >= 3 ? m[L >= 3 ? L - 3 : 0] : 0u;
+  uint32_t rest = 0;
+#pragma unroll
+  for (int u = 0; u + 3 < L; u++) rest |= m[u];
+  const uint64_t T = ((uint64_t)__funnelshift_l(mid, hi, lz) << 32) | __funnelshift_l(lo, mid, lz);
+  const uint64_t kept = T >> (64 - F::prec);
+  const uint32_t round = (uint32_t)(T >> (63 - F::prec)) & 1u;
+  const bool sticky = (T & ((1ull << (63 - F::prec)) - 1)) != 0 || (lo << lz) != 0 || rest != 0;
+  const uint32_t inc = round & ((sticky ? 1u : 0u) | (uint32_t)kept);
+  return F::pack_normal(kept + inc, etop, neg);
 }
 
 // Exact float of x < 2^23 from its bit pattern.

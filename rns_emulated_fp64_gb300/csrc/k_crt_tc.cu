@@ -27,13 +27,16 @@
 //   - round X 2^-(e_i + f_j) once to nearest-even ([Q] "2の累乗による整数化(手順1と5)").
 // The results are bit-identical to the CUDA-core kernel (k_crt.cu).
 //
-// Layout: a persistent CTA of 4 warps takes rounds of 512 consecutive entries of
-// one row of C.  Each warp reads moduli l = warp, warp + 4, ... as 16-byte loads
+// Layout: a persistent CTA of 8 warps takes rounds of 512 consecutive entries of
+// one row of C.  Each warp reads moduli l = warp, warp + 8, ... as 16-byte loads
 // (32 lanes x 16 entries), widens them into an MN-major, 128-byte-swizzled FP16
 // tile (entries contiguous, one 8-row atom per 8 moduli), and one thread issues
 // four MMAs of 128 entries into TMEM.  Rounds are double-buffered in shared
 // memory and TMEM: the next round's loads and MMAs run while the warps fold the
-// previous round's digit sums (tcgen05.ld: lane = entry, columns = digits).
+// previous round's digit sums (tcgen05.ld: lane = entry, columns = digits; a
+// warp reads its TMEM lane quarter of two of the four tiles, so each thread
+// reconstructs two independent entries per round, their exponents loaded one
+// round ahead).
 // Every wait is bounded; on expiry the CTA records OS2_ERR_TIMEOUT, waits once
 // more (bounded) for its MMAs, frees its TMEM and returns.
 #include <cuda_fp16.h>
@@ -49,7 +52,8 @@ using namespace os2crt;
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kU = 4;                 // MMA tiles of 128 entries per round
 constexpr int kSeg = 128 * kU;        // entries per round
 constexpr long long kWait = 4000000000LL;  // clock cycles (about 2 s)
@@ -71,7 +75,7 @@ struct Shape {
   static constexpr int NMMA = N <= 16 ? 16 : 32;        // digit columns (>= T)
   static constexpr int T = kDigits[N], Q = kQDigits[N];
   static constexpr int LX = kLimbs[N];
-  static constexpr int MPW = (N + 3) / 4;               // moduli per warp
+  static constexpr int MPW = (N + kWarps - 1) / kWarps; // moduli each warp loads
   static constexpr uint32_t SBO = 2048;                 // 8-modulus atoms, 2 x 1024 B apart
   static constexpr uint32_t A_TILE = 128 * KPAD * 2;    // one MMA's A (bytes)
   static constexpr uint32_t A_BUF = kU * A_TILE;
@@ -131,15 +135,12 @@ __device__ __forceinline__ void finish_entry(const uint32_t *v, const CrtTcConst
   float tq = cc.c0;
 #pragma unroll
   for (int j = Q - 1; j >= 0; j--) tq = fmaf(dq[j], cc.s[j], tq);
+  // Y >= 0, so tq >= -128/P - 0.003 and the rounded q is never negative
   const float tr = tq + 12582912.0f;
-  int qi = __float_as_int(tr) - 0x4B400000;
-  float qf = tr - 12582912.0f;
-  if (qi < 0) {  // only when Y - 128 is within rounding of -P/2 (then q = 0)
-    qi = 0;
-    qf = 0.0f;
-  }
+  const uint32_t qi = (uint32_t)(__float_as_int(tr) - 0x4B400000);
+  const float qf = tr - 12582912.0f;
 #pragma unroll
-  for (int u = 0; u < LX; u++) acc[u] += (uint64_t)(uint32_t)qi * cc.np[u];
+  for (int u = 0; u < LX; u++) acc[u] += (uint64_t)qi * cc.np[u];
   uint32_t x[LX];
   uint64_t cy = 0;
 #pragma unroll
@@ -172,32 +173,29 @@ __device__ __forceinline__ void finish_entry(const uint32_t *v, const CrtTcConst
       }
     }
   }
-  const bool neg = (int32_t)x[LX - 1] < 0;
+  const uint32_t sm = (uint32_t)((int32_t)x[LX - 1] >> 31);  // all ones if X < 0
   if (xo) {
 #pragma unroll
-    for (int u = 0; u < 8; u++) xo[u] = u < LX ? x[u < LX ? u : 0] : (neg ? 0xFFFFFFFFu : 0u);
+    for (int u = 0; u < 8; u++) xo[u] = u < LX ? x[u < LX ? u : 0] : sm;
   }
+  // |X| = (X xor sm) - sm
   uint32_t mag[LX];
-  if (neg) {
-    uint64_t c1 = 1;
+  uint64_t c1 = sm & 1u;
 #pragma unroll
-    for (int u = 0; u < LX; u++) {
-      c1 += (uint64_t)(~x[u]);
-      mag[u] = (uint32_t)c1;
-      c1 >>= 32;
-    }
-  } else {
-#pragma unroll
-    for (int u = 0; u < LX; u++) mag[u] = x[u];
+  for (int u = 0; u < LX; u++) {
+    c1 += (uint64_t)(x[u] ^ sm);
+    mag[u] = (uint32_t)c1;
+    c1 >>= 32;
   }
-  *dst = round_scaled_fast<OutT, LX>(mag, neg, s_exp);
+  *dst = round_scaled_top<OutT, LX>(mag, sm != 0, s_exp);
 }
 
 template <int N, typename OutT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 512 / (2 * kU * Shape<N>::NMMA))
     k_crt_tc(int m, int n, int segs, int rounds, const int8_t *__restrict__ c, int ldcres,
              const int32_t *__restrict__ e, const int32_t *__restrict__ f, OutT *__restrict__ C,
-             int ldc, uint32_t *__restrict__ Xout, const CrtTcConsts cc, int *status) {
+             int ldc, uint32_t *__restrict__ Xout, const __grid_constant__ CrtTcConsts cc,
+             int *status) {
   using S = Shape<N>;
   constexpr int NMMA = S::NMMA, MPW = S::MPW;
   constexpr uint32_t IDESC = idesc_f16_f32(128, NMMA) | (1u << 15);  // A MN-major
@@ -236,18 +234,31 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t tmem_base = *s_tmem;
   const size_t plane = (size_t)m * ldcres;
 
-  // this lane's 16 entries of a round: tile u, entries e0 .. e0+15 of it
+  // loads: this lane's 16 entries of a round (tile u, entries e0 .. e0+15 of
+  // it) of moduli warp, warp + 8, ...
   const int eR = 16 * lane;
   const int tile = eR >> 7, e0 = eR & 127;
+  // reconstruction: TMEM lane quarter `quarter`, tiles 2 half and 2 half + 1
+  const int quarter = warp & 3, half = warp >> 2;
   uint4 raw[MPW];
-  auto load = [&](int r) {
-    const int i = r / segs, j = (r - i * segs) * kSeg + eR;
+  auto load = [&](int i, int sg) {
+    const int j = sg * kSeg + eR;
     const int8_t *src = c + (size_t)i * ldcres + j;
 #pragma unroll
     for (int q = 0; q < MPW; q++) {
-      const int l = warp + 4 * q;
+      const int l = warp + kWarps * q;
       raw[q] = (l < N && j < ldcres) ? ldg16(src + (size_t)(l < N ? l : 0) * plane)
                                      : make_uint4(0, 0, 0, 0);
+    }
+  };
+  // exponent sums e_i + f_j of this thread's two entries of a round
+  auto load_exp = [&](int i, int sg, int (&ef)[2]) {
+    const int jr = sg * kSeg;
+    const int ei = __ldg(e + i);
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const int j = jr + (2 * half + h) * 128 + quarter * 32 + lane;
+      ef[h] = j < n ? ei + __ldg(f + j) : 0;
     }
   };
   auto stage = [&](int buf) {
@@ -255,7 +266,7 @@ __global__ void __launch_bounds__(kThreads)
     const int ch = (e0 >> 3) & 7;  // even: this lane's two 16-byte chunks are ch, ch + 1
 #pragma unroll
     for (int q = 0; q < MPW; q++) {
-      const int l = warp + 4 * q;
+      const int l = warp + kWarps * q;
       if (l < N) {
         uint32_t h[8];
         widen4(raw[q].x, h[0], h[1]);
@@ -281,23 +292,26 @@ __global__ void __launch_bounds__(kThreads)
     }
     umma_commit(&bars[buf]);
   };
-  auto post = [&](int r, int buf) {
-    const int i = r / segs, jr = (r - i * segs) * kSeg;
-    const int ei = e[i];
-#pragma unroll 1
-    for (int u = 0; u < kU; u++) {
-      const int j = jr + u * 128 + warp * 32 + lane;
-      const uint32_t taddr =
-          tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)((buf * kU + u) * NMMA);
-      uint32_t v[NMMA];
-      if (NMMA == 16) {
-        tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
-      } else {
-        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
-      }
-      tmem_wait_ld();
+  // this thread's two entries of round r: both TMEM loads, one wait, then
+  // the two independent reconstructions
+  auto post = [&](int i, int sg, int buf, const int (&ef)[2]) {
+    const int jr = sg * kSeg;
+    uint32_t v[2][NMMA];
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                             (uint32_t)((buf * kU + 2 * half + h) * NMMA);
+      if (NMMA == 16)
+        tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v[h]));
+      else
+        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v[h]));
+    }
+    tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const int j = jr + (2 * half + h) * 128 + quarter * 32 + lane;
       if (j < n)
-        finish_entry<N, OutT>(v, cc, ei + f[j], C + (size_t)i * ldc + j,
+        finish_entry<N, OutT>(v[h], cc, ef[h], C + (size_t)i * ldc + j,
                               Xout ? Xout + ((size_t)i * n + j) * 8 : nullptr);
     }
   };
@@ -306,31 +320,50 @@ __global__ void __launch_bounds__(kThreads)
   bool ok = true;
   int it = 0;
   int r = blockIdx.x;
-  if (r < rounds) load(r);
+  int ef_post[2] = {0, 0}, ef_next[2] = {0, 0};
+  // round r = i * segs + sg, stepped by the grid without divisions
+  const int di = (int)gridDim.x / segs, ds = (int)gridDim.x - di * segs;
+  int ci = r / segs, cs = r - ci * segs;  // round r
+  int pi = 0, ps = 0;                     // the round before it
+  if (r < rounds) load(ci, cs);
   for (; r < rounds; r += gridDim.x, it++) {
     const int buf = it & 1;
     stage(buf);  // the MMAs that last read this buffer completed (waited on in post)
-    if (r + (int)gridDim.x < rounds) load(r + gridDim.x);
     fence_async_smem();
     tc_fence_before();
     ok = __syncthreads_and(ok);
     if (!ok) break;
     tc_fence_after();
     if (threadIdx.x == 0) issue(buf);
+    // next round's residues and this round's exponents: issued after the
+    // proxy fence (which may wait for outstanding memory operations), in
+    // flight while the previous round is reconstructed
+    int ni = ci + di, ns = cs + ds;
+    if (ns >= segs) {
+      ns -= segs;
+      ni++;
+    }
+    if (r + (int)gridDim.x < rounds) load(ni, ns);
+    ef_post[0] = ef_next[0];
+    ef_post[1] = ef_next[1];
+    load_exp(ci, cs, ef_next);  // used one iteration later, by post of this round
     if (it > 0) {
       if (mbar_wait_bounded(&bars[buf ^ 1], ((it - 1) >> 1) & 1, &no_abort, kWait)) {
         tc_fence_after();
-        post(r - gridDim.x, buf ^ 1);
+        post(pi, ps, buf ^ 1, ef_post);
       } else {
         ok = false;
       }
     }
+    pi = ci;
+    ps = cs;
+    ci = ni;
+    cs = ns;
   }
   if (ok && it > 0) {
-    const int last = blockIdx.x + (it - 1) * gridDim.x;
     if (mbar_wait_bounded(&bars[(it - 1) & 1], ((it - 1) >> 1) & 1, &no_abort, kWait)) {
       tc_fence_after();
-      post(last, (it - 1) & 1);
+      post(pi, ps, (it - 1) & 1, ef_next);
     } else {
       ok = false;
     }
