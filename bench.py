@@ -61,8 +61,11 @@ def parse():
                     help="skip the N in {14,16,18} x {fast, accurate} sweep of the same workload")
     ap.add_argument("--no-peaks", action="store_true",
                     help="skip the tensor-pipe peak probes (own kernels) before the timed steps")
-    ap.add_argument("--crt", default="default", choices=["default", "tc", "simt"],
+    ap.add_argument("--crt", default="default", choices=["default", "tc", "simt", "auto"],
                     help="kernel of steps 4 + 5 (os2_set_crt_variant); default: the library's")
+    ap.add_argument("--accuracy", action="store_true",
+                    help="error against the exact product for 1024^3, phi in {0.5,2,4}, N in "
+                         "{12..20}, both modes, beside native DGEMM; prints one JSON line")
     ap.add_argument("--peaks-only", action="store_true",
                     help="run only the tensor-pipe peak probes and print them as one JSON line")
     return ap.parse_args()
@@ -328,7 +331,7 @@ def run_ours(a):
     world, rank, local = dist_setup(a)
     dev = torch.device("cuda", local if world > 1 else 0)
     if a.crt != "default":
-        os2.set_crt_variant(os2.CRT_TC if a.crt == "tc" else os2.CRT_SIMT)
+        os2.set_crt_variant({"tc": os2.CRT_TC, "simt": os2.CRT_SIMT, "auto": os2.CRT_AUTO}[a.crt])
     m, n, k, N = a.m, a.n, a.k, a.num_moduli
     A, Bt = workloads.make_pair("spread", m, n, k, seed=rank, phi=a.phi)
     Ad = torch.from_numpy(A).to(dev)
@@ -452,19 +455,33 @@ def run_ours(a):
         # other tenants, so the spread of single calls is reported beside the mean
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(ke + 1)]
         e0, e1 = evs[0], evs[-1]
+        host_ms = []
         e0.record(stream)
         for i in range(ke):
+            h0 = time.perf_counter()
             os2.gemm_host(Ah, Bh, Ch, N, a.mode, workspace=wsh, stream=stream)
+            host_ms.append(1e3 * (time.perf_counter() - h0))  # enqueue only: the call is async
             evs[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-        calls = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(ke))
+        per_call = [evs[i].elapsed_time(evs[i + 1]) for i in range(ke)]
+        calls = sorted(per_call)
         barrier(world)
         ems, evalue = aggregate(world, e0.elapsed_time(e1), flop, ke)
+        med = calls[len(calls) // 2]
+        hmed = sorted(host_ms)[len(host_ms) // 2]
+        slow = [{"call": i, "device_ms": per_call[i], "host_enqueue_ms": host_ms[i],
+                 "host_enqueue_slow": host_ms[i] > max(5 * hmed, hmed + 1.0)}
+                for i in range(ke) if per_call[i] > 1.5 * med]
+        trimmed = (sum(per_call) - calls[-1]) / (ke - 1) if ke > 1 else per_call[0]
         line["e2e"] = {"value": evalue, "unit": UNIT,
                        "h2d_bytes_per_step": 8 * (m * k + n * k), "d2h_bytes_per_step": 8 * m * n,
                        "steps": ke, "ms_per_step": ems / ke,
-                       "call_ms": {"min": calls[0], "median": calls[len(calls) // 2],
-                                   "max": calls[-1]}}
+                       "call_ms": {"min": calls[0], "median": med, "max": calls[-1],
+                                   "mean": sum(per_call) / ke,
+                                   "mean_without_slowest": trimmed,
+                                   "tflops_without_slowest": flop / (trimmed / 1e3) / 1e12},
+                       "host_enqueue_ms": {"median": hmed, "max": max(host_ms)},
+                       "slow_calls": slow}
         assert torch.equal(Ch, Cd.cpu()), "host entry point result differs from device entry point"
         del wsh
 
@@ -555,21 +572,22 @@ def run_ours(a):
         t1.record(stream)
         torch.cuda.synchronize(dev)
         nat_ms = t0.elapsed_time(t1)
-        rr, cc = workloads.sample_grid(m, n, 6, seed=2)
-        Ce = Cd.cpu().numpy()
-        Cnn = Cn.cpu().numpy()
-        e_emu = e_nat = 0.0
-        for i in rr:
-            for j in cc:
-                ex = exact_dot(A[i], Bt[j])
-                scale = float(np.abs(A[i]) @ np.abs(Bt[j]))
-                e_emu = max(e_emu, abs(Ce[i, j] - ex) / scale)
-                e_nat = max(e_nat, abs(Cnn[i, j] - ex) / scale)
+        rr, cc = workloads.sample_grid(m, n, 16, seed=2)
+        ex, scale = exact_products(A, Bt, rr, cc)
+        errs = {"native_dgemm": rel_errors(Cn.cpu().numpy()[np.ix_(rr, cc)], ex, scale)}
+        errs[f"N{N}_{a.mode}"] = rel_errors(Cd.cpu().numpy()[np.ix_(rr, cc)], ex, scale)
+        for Ns in (14, 16, 18):
+            if Ns != N:
+                wse = os2.alloc_workspace(os2.workspace_size(m, n, k, Ns, a.mode), dev)
+                Cs = os2.gemm(Ad, Bd, Ns, a.mode, workspace=wse, stream=stream)
+                errs[f"N{Ns}_{a.mode}"] = rel_errors(Cs.cpu().numpy()[np.ix_(rr, cc)], ex, scale)
+                del wse, Cs
+                torch.cuda.empty_cache()
         line["context"] = {"native_dgemm_tflops": flop / (nat_ms / 1e3) / 1e12,
                            "native_dgemm": "torch.matmul float64 (cuBLAS DGEMM)",
-                           "max_err_over_absprod_emulated": e_emu,
-                           "max_err_over_absprod_native": e_nat,
-                           "error_sample": f"{len(rr)}x{len(cc)} entries vs exact (fsum)"}
+                           "err_over_absprod_max_median": errs,
+                           "error_sample": f"{len(rr)}x{len(cc)} entries vs the exact product "
+                                           "(Dekker products, fsum)"}
         del Cn
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -595,8 +613,54 @@ def run_peaks_only(a):
     print(json.dumps({"pipe_peaks": out}), flush=True)
 
 
+def exact_products(A, Bt, rows, cols):
+    """Correctly rounded (AB)_ij and (|A||B|)_ij on a grid of entries."""
+    ex = np.array([[exact_dot(A[i], Bt[j]) for j in cols] for i in rows])
+    scale = np.abs(A[rows]) @ np.abs(Bt[cols]).T
+    return ex, scale
+
+
+def rel_errors(C, ex, scale):
+    r = np.abs(C - ex) / np.where(scale > 0, scale, 1.0)
+    return float(r.max()), float(np.median(r))
+
+
+def run_accuracy(a):
+    """Error of the emulated product against the exact one, per config of the
+    1024^3 workload, with native cuBLAS DGEMM beside it."""
+    import torch
+
+    import rns_emulated_fp64_gb300 as os2
+    torch.cuda.set_device(0)
+    m = n = k = 1024
+    rows, cols = workloads.sample_grid(m, n, 64, seed=1)
+    out = {"workload": "1024x1024x1024 FP64, entries (U(0,1)-0.5)*exp(phi*N(0,1)), seed 0",
+           "sample": f"{len(rows)} x {len(cols)} entries (seeded grid, last row and column "
+                     "included) against the exact product (Dekker products, fsum)",
+           "error": "|C_ij - (AB)_ij| / (|A||B|)_ij", "configs": {}}
+    for phi in (0.5, 2.0, 4.0):
+        A, Bt = workloads.make_pair("spread", m, n, k, seed=0, phi=phi)
+        ex, scale = exact_products(A, Bt, rows, cols)
+        Ad, Bd = torch.from_numpy(A).cuda(), torch.from_numpy(Bt).cuda()
+        nat = torch.matmul(Ad, Bd.t()).cpu().numpy()[np.ix_(rows, cols)]
+        mx, md = rel_errors(nat, ex, scale)
+        rec = {"native_dgemm": {"max": mx, "median": md}}
+        for N in range(12, 21, 2):
+            for mode in ("fast", "accurate"):
+                C = os2.gemm(Ad, Bd, N, mode).cpu().numpy()[np.ix_(rows, cols)]
+                if os2.get_status():
+                    raise RuntimeError("device status set")
+                mx, md = rel_errors(C, ex, scale)
+                rec[f"N{N}_{mode}"] = {"max": mx, "median": md}
+        out["configs"][f"phi{phi}"] = rec
+    print(json.dumps({"accuracy": out}), flush=True)
+
+
 def main():
     a = parse()
+    if a.accuracy:
+        run_accuracy(a)
+        return
     if a.peaks_only:
         run_peaks_only(a)
         return

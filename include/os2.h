@@ -77,8 +77,9 @@ typedef enum {
 } os2_gemm_variant;
 
 typedef enum {
-  OS2_CRT_TC = 0,         /* limb sums as an FP16 tensor-core MMA per 128 entries (default) */
-  OS2_CRT_SIMT = 1        /* limb sums as 32x32->64 multiply-adds on the CUDA cores */
+  OS2_CRT_TC = 0,         /* limb sums as an FP16 tensor-core MMA per 128 entries */
+  OS2_CRT_SIMT = 1,       /* limb sums as 32x32->64 multiply-adds on the CUDA cores */
+  OS2_CRT_AUTO = 2        /* (default) TC alone; SIMT beside a product (see below) */
 } os2_crt_variant;
 
 typedef enum {
@@ -95,15 +96,14 @@ size_t os2_workspace_size(int m, int n, int k, int num_moduli, int mode);
 /* The whole five-step emulated DGEMM, C = A*B ([Q] "行列積への当てはめ方": the
  * five steps applied to a matrix product; step 1 in fast mode follows [G]
  * "Methodik").  Layouts above.  Returns after
- * enqueueing on `stream`.  With the default reconstruction kernel
- * (OS2_CRT_TC) every step runs on `stream`, once over the whole problem.
- * With OS2_CRT_SIMT (os2_set_crt_variant) and m >= 4096 the rows of A go in
- * panels of about 2048: the CRT and unscaling of one panel run on a
- * library-owned stream (created once per device, non-blocking) beside the
- * product of the next; that stream first waits for the work already on
- * `stream`, and `stream` waits for it before the call's work ends, so
- * synchronising `stream` covers the call.  Results are identical either way.
- * Calls from several host threads are enqueued one at a time. */
+ * enqueueing on `stream`.  For m >= 4096 (unless os2_set_crt_variant selected
+ * OS2_CRT_TC) the rows of A go in panels of about 2048: the CRT and unscaling
+ * of one panel run on a library-owned stream (created once per device,
+ * non-blocking) beside the product of the next; that stream first waits for
+ * the work already on `stream`, and `stream` waits for it before the call's
+ * work ends, so synchronising `stream` covers the call.  Otherwise every step
+ * runs on `stream`, once over the whole problem.  Results are identical
+ * either way.  Calls from several host threads are enqueued one at a time. */
 os2_status os2_gemm(int m, int n, int k, const double *A, int lda, const double *B, int ldb,
                     double *C, int ldc, int num_moduli, int mode, void *workspace,
                     size_t workspace_bytes, void *stream);
@@ -169,6 +169,44 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
                      int num_moduli, int mode, int32_t *e, int32_t *f, void *workspace,
                      size_t workspace_bytes, void *stream);
 
+/* Accurate-mode step 1 split in two, for a product computed in output blocks
+ * (one block per GPU, [Q] "誤差のないINT8行列積(手順3)": the moduli, the
+ * residues and the reconstruction are independent per entry, and the scaling
+ * is per row and per column).  os2_scale_bounds takes the block's rows of A
+ * and columns of B (layouts as os2_gemm) and writes, as device int32 arrays:
+ * R[m] = max_j Cbar_ij over the block's columns, K[n] = max_i Cbar_ij over its
+ * rows (Cbar = Abar Bbar, the exact product of the 6-bit magnitude planes of
+ * the accurate mode), and the exponent bases EA[m], EB[n] (|a_ih| < 2^EA_i; 0
+ * for a row of zeros).  Workspace: os2_workspace_size(m, n, k, 1,
+ * OS2_MODE_ACCURATE) bytes, 256-byte aligned.  The maxima of the whole product
+ * are the MAX over the blocks that share the rows (R) or the columns (K); the
+ * exponents then follow from os2_exponents_from_bounds, identical to those
+ * os2_scale computes for the whole product.  k < 2^19 (else
+ * OS2_ERR_UNSUPPORTED). */
+os2_status os2_scale_bounds(int m, int n, int k, const double *A, int lda, const double *B,
+                            int ldb, int32_t *R, int32_t *K, int32_t *EA, int32_t *EB,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Accurate-mode exponents e[i] = 6 - E[i] + (largest g with bound[i] 4^g <= H),
+ * e[i] = -E[i] for bound[i] = 0 ([Q] "2の累乗による整数化(手順1と5)", with the
+ * bound of one extra exact product), for `count` rows or columns; device
+ * int32 arrays. */
+os2_status os2_exponents_from_bounds(int count, const int32_t *bound, const int32_t *E,
+                                     int num_moduli, int32_t *e, void *stream);
+
+/* Steps 2 to 5 with the exponents given (e[m] for A's rows, f[n] for B's
+ * columns, device int32), for example those of os2_scale or
+ * os2_exponents_from_bounds for a block of a larger product.  Arguments,
+ * layouts, workspace (os2_workspace_size(m, n, k, N, OS2_MODE_FAST)) and
+ * errors as os2_gemm.  Exponents larger than the scaling's can push the
+ * integer product past P/2, where the reconstruction wraps: the result is
+ * then unspecified (and OS2_ERR_RANGE is set if a scaled entry reaches
+ * 2^89). */
+os2_status os2_gemm_exponents(int m, int n, int k, const double *A, int lda, const double *B,
+                              int ldb, double *C, int ldc, int num_moduli, const int32_t *e,
+                              const int32_t *f, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
 /* Step 2 alone for one operand ([Q] "2の累乗による整数化(手順1と5)": truncation of
  * the scaled entries to integers; [Q] "256以下の法の選び方(手順2)": their
  * symmetric residues, for p = 256 the low byte read as int8): rows x k
@@ -233,14 +271,18 @@ os2_status os2_get_status(void *stream);
  * for a limit out of range (nothing enqueued). */
 os2_status os2_wait_selftest(long long limit_cycles, int32_t *result, void *stream);
 
-/* Selects the kernel of steps 4 and 5 (process-wide; default OS2_CRT_TC).
- * Both give bit-identical results.  OS2_CRT_TC computes the sums
+/* Selects the kernel of steps 4 and 5 (process-wide; default OS2_CRT_AUTO).
+ * All give bit-identical results.  OS2_CRT_TC computes the sums
  * sum_l (c_l + 128) W_l as an FP16 tensor-core product of the residues with
  * the signed 10-bit digits of the W_l, exact in FP32; it needs rows of c that
- * are 16-byte aligned (os2_crt falls back to OS2_CRT_SIMT otherwise).  With
- * OS2_CRT_TC, os2_gemm runs in one pass (one product launch); with
- * OS2_CRT_SIMT it cuts A into row panels for m >= 4096 and runs each panel's
- * reconstruction on the CUDA cores beside the next panel's product.
+ * are 16-byte aligned (the CUDA-core kernel is used otherwise).  It cannot run
+ * beside a product (it needs TMEM and shared memory a product CTA holds), so
+ * with OS2_CRT_TC os2_gemm runs in one pass (one product launch).  With
+ * OS2_CRT_SIMT, os2_gemm cuts A into row panels for m >= 4096 and runs each
+ * panel's reconstruction on the CUDA cores beside the next panel's product,
+ * and os2_gemm_host does the same per block.  OS2_CRT_AUTO: the panels and
+ * blocks as with OS2_CRT_SIMT, and the tensor-core kernel for every
+ * reconstruction that runs alone (os2_crt, os2_gemm with one panel).
  * OS2_ERR_INVALID_ARG for another value. */
 os2_status os2_set_crt_variant(int variant);
 

@@ -59,6 +59,8 @@ def load():
             lib.orc_crt_small.argtypes = [i32, P, P, P]
             lib.orc_scale_fast.argtypes = [i32, i32, P, l, i32, P, P]
             lib.orc_scale_accu.argtypes = [i32, i32, i32, P, l, P, l, i32, i32, P, P, i32, P, P, P, P]
+            lib.orc_row_exponents.argtypes = [i32, i32, P, l, P]
+            lib.orc_exps_from_bounds.argtypes = [i32, P, P, i32, P]
             lib.orc_integers.argtypes = [i32, i32, P, l, P, P]
             lib.orc_residues.argtypes = [i32, i32, P, l, P, i32, P]
             lib.orc_round_scaled.argtypes = [P, i32]
@@ -192,6 +194,28 @@ def scale_accu(A, Bt, N: int, rows=None, cols=None, return_bounds: bool = False)
                                  _ptr(e), len(cols), _ptr(cols), _ptr(f), _ptr(R), _ptr(K)),
            "orc_scale_accu")
     return (e, f, R, K) if return_bounds else (e, f)
+
+
+def row_exponents(X):
+    """Exponent bases E_i of the rows of X (|x_ih| < 2^E_i, 0 for a zero row),
+    as the accurate mode uses them."""
+    X, ld = _rows(X)
+    E = np.zeros(X.shape[0], np.int32)
+    _check(load().orc_row_exponents(X.shape[0], X.shape[1], _ptr(X), ld, _ptr(E)),
+           "orc_row_exponents")
+    return E
+
+
+def exps_from_bounds(R, E, N: int):
+    """Accurate-mode exponents from bounds R and exponent bases E (the last
+    step of ``scale_accu``, for bounds reduced across the blocks of a split
+    product)."""
+    R = np.ascontiguousarray(R, np.int64)
+    E = np.ascontiguousarray(E, np.int32)
+    e = np.zeros(len(R), np.int32)
+    _check(load().orc_exps_from_bounds(len(R), _ptr(R), _ptr(E), N, _ptr(e)),
+           "orc_exps_from_bounds")
+    return e
 
 
 def integers(X, e):

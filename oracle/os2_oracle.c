@@ -428,6 +428,32 @@ int orc_scale_accu(int m, int n, int k, const double *A, long lda, const double 
   return err;
 }
 
+/* The two ends of orc_scale_accu as separate calls, for bounds gathered
+ * elsewhere -- for example the maxima R_i, K_j of a product split into output
+ * blocks, each block's maxima taken over its own columns (rows) and then
+ * reduced with MAX over the blocks that share its rows (columns).
+ * orc_row_exponents: the exponent bases E_i (|x_ih| < 2^E_i; 0 for a row of
+ * zeros).  orc_exps_from_bounds: e = g(R) + 6 - E (e = -E for R = 0). */
+int orc_row_exponents(int rows, int k, const double *X, long ldx, int32_t *E) {
+  int err = ORC_OK;
+  for (int i = 0; i < rows && !err; i++) {
+    int Ei, nz;
+    err = row_max_exp(X + (long)i * ldx, k, &Ei, &nz);
+    E[i] = Ei;
+  }
+  return err;
+}
+
+int orc_exps_from_bounds(int cnt, const int64_t *R, const int32_t *E, int N, int32_t *e) {
+  orc_tables_t t;
+  if (make_tables(N, &t)) return ORC_ERR_ARG;
+  for (int i = 0; i < cnt; i++) {
+    if (R[i] < 0) return ORC_ERR_ARG;
+    e[i] = exp_from_bound(R[i], E[i], &t);
+  }
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Step 2 -- truncation to integers and symmetric residues                    */
 /* ------------------------------------------------------------------------- */

@@ -10,4 +10,5 @@ from .binding import (GEMM_SIMT, GEMM_TC, GEMM_TC_1SM, MODE_ACCURATE, MODE_FAST,
                       set_gemm_variant, status_string, workspace_size, zgemm,
                       complex_workspace_size, wait_selftest, ERR_TIMEOUT, peak_probe,
                       PROBE_F16_1SM, PROBE_F16_2SM, PROBE_S8_SYNC, set_crt_variant,
-                      CRT_TC, CRT_SIMT)
+                      CRT_TC, CRT_SIMT, CRT_AUTO, scale_bounds, exponents_from_bounds,
+                      gemm_exponents)

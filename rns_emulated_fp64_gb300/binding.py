@@ -18,7 +18,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, 1, 2, 3
 ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA = 4, 5, 6, 7
 MODE_FAST, MODE_ACCURATE = 0, 1
 GEMM_TC, GEMM_SIMT, GEMM_TC_1SM = 0, 1, 2
-CRT_TC, CRT_SIMT = 0, 1
+CRT_TC, CRT_SIMT, CRT_AUTO = 0, 1, 2
 OUT_MODP_INT8, OUT_RAW_INT32 = 0, 1
 KP_ALIGN, CRES_ALIGN = 64, 16
 
@@ -28,7 +28,8 @@ EXPORTS = ("os2_workspace_size", "os2_gemm", "os2_host_workspace_size", "os2_gem
            "os2_get_status", "os2_set_gemm_variant", "os2_status_string",
            "os2_gemm_launch_count", "os2_profile_start", "os2_profile_stop",
            "os2_gemm_noalloc", "os2_sgemm", "os2_complex_workspace_size", "os2_zgemm",
-           "os2_cgemm", "os2_wait_selftest", "os2_peak_probe", "os2_set_crt_variant")
+           "os2_cgemm", "os2_wait_selftest", "os2_peak_probe", "os2_set_crt_variant",
+           "os2_scale_bounds", "os2_exponents_from_bounds", "os2_gemm_exponents")
 
 _lib = None
 _lock = threading.Lock()
@@ -103,6 +104,12 @@ def load(build_if_missing: bool = True):
         L.os2_peak_probe.restype = i
         L.os2_set_crt_variant.argtypes = [i]
         L.os2_set_crt_variant.restype = i
+        L.os2_scale_bounds.argtypes = [i, i, i, d, i, d, i, vp, vp, vp, vp, vp, sz, vp]
+        L.os2_scale_bounds.restype = i
+        L.os2_exponents_from_bounds.argtypes = [i, vp, vp, i, vp, vp]
+        L.os2_exponents_from_bounds.restype = i
+        L.os2_gemm_exponents.argtypes = [i, i, i, d, i, d, i, d, i, i, vp, vp, vp, sz, vp]
+        L.os2_gemm_exponents.restype = i
         _lib = L
         return L
 
@@ -170,8 +177,9 @@ def set_gemm_variant(variant: int):
 
 
 def set_crt_variant(variant: int):
-    """Kernel of steps 4 + 5: CRT_TC (tensor-core limb sums, default) or
-    CRT_SIMT (CUDA-core multiply-adds); results are bit-identical."""
+    """Kernel of steps 4 + 5: CRT_TC (tensor-core limb sums), CRT_SIMT
+    (CUDA-core multiply-adds) or CRT_AUTO (the default: CUDA cores beside a
+    product, tensor cores alone); results are bit-identical."""
     _check(load().os2_set_crt_variant(int(variant)), "os2_set_crt_variant")
 
 
@@ -390,6 +398,54 @@ def profile_stop() -> dict:
         raise Os2Error(ERR_CUDA, "os2_profile_stop")
     raw = names.raw
     return {raw[32 * i:32 * i + 32].split(b"\0")[0].decode(): (tot[i], cnt[i]) for i in range(n)}
+
+
+def scale_bounds(A: torch.Tensor, Bt: torch.Tensor, workspace=None, stream=None):
+    """Accurate-mode bound maxima of a block: (R, K, EA, EB), int32 CUDA
+    tensors (see os2_scale_bounds)."""
+    A, lda = _kmat(A, "A")
+    Bt, ldb = _kmat(Bt, "Bt")
+    m, k = A.shape
+    n = Bt.shape[0]
+    dev = A.device
+    R = torch.empty(m, dtype=torch.int32, device=dev)
+    K = torch.empty(n, dtype=torch.int32, device=dev)
+    EA = torch.empty(m, dtype=torch.int32, device=dev)
+    EB = torch.empty(n, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(m, n, k, 1, "accurate"), dev)
+    _check(load().os2_scale_bounds(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, _ptr(R), _ptr(K),
+                                   _ptr(EA), _ptr(EB), _ptr(workspace), workspace.numel(),
+                                   _stream(stream)), "os2_scale_bounds")
+    return R, K, EA, EB
+
+
+def exponents_from_bounds(bound: torch.Tensor, E: torch.Tensor, num_moduli: int, stream=None):
+    """Accurate-mode exponents from bounds and exponent bases (int32 CUDA)."""
+    bound = bound.to(torch.int32).contiguous()
+    E = E.to(torch.int32).contiguous()
+    e = torch.empty_like(E)
+    _check(load().os2_exponents_from_bounds(bound.numel(), _ptr(bound), _ptr(E), int(num_moduli),
+                                            _ptr(e), _stream(stream)), "os2_exponents_from_bounds")
+    return e
+
+
+def gemm_exponents(A: torch.Tensor, Bt: torch.Tensor, num_moduli: int, e: torch.Tensor,
+                   f: torch.Tensor, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Steps 2-5 with given exponents e (rows of A) and f (columns = rows of Bt)."""
+    A, lda = _kmat(A, "A")
+    Bt, ldb = _kmat(Bt, "Bt")
+    m, k = A.shape
+    n = Bt.shape[0]
+    C = out if out is not None else torch.empty((m, n), dtype=torch.float64, device=A.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size(m, n, k, num_moduli, "fast"), A.device)
+    e = e.to(torch.int32).contiguous()
+    f = f.to(torch.int32).contiguous()
+    _check(load().os2_gemm_exponents(m, n, k, _ptr(A), lda, _ptr(Bt), ldb, _ptr(C), C.stride(0),
+                                     int(num_moduli), _ptr(e), _ptr(f), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "os2_gemm_exponents")
+    return C
 
 
 NOALLOC_SCRATCH_BYTES = 128 << 20

@@ -283,7 +283,7 @@ void build_tables(int N, Os2Tables *t) {
 }
 
 std::atomic<int> g_variant{OS2_GEMM_TC};
-std::atomic<int> g_crt_variant{OS2_CRT_TC};
+std::atomic<int> g_crt_variant{OS2_CRT_AUTO};
 
 // Optional per-kernel timing: CUDA events recorded on the launching stream
 // around every kernel that os2_gemm enqueues (no synchronisation added).
@@ -374,15 +374,18 @@ bool make_layout(int m, int n, int k, int N, int mode, Layout *L) {
 os2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OS2_OK : OS2_ERR_CUDA; }
 
 // Steps 4 + 5 on the selected kernel: the tensor-core one needs 16-byte rows
-// of the product residues (always so inside the library).
-bool crt_on_tc(int ldcres, const void *c) {
-  return g_crt_variant.load() == OS2_CRT_TC && ldcres % 16 == 0 &&
+// of the product residues (always so inside the library).  AUTO takes it for
+// a reconstruction that runs alone; `beside` marks one that runs beside a
+// product (row panels, host-path blocks), which takes the CUDA-core kernel.
+bool crt_on_tc(int ldcres, const void *c, bool beside = false) {
+  const int v = g_crt_variant.load();
+  return (v == OS2_CRT_TC || (v == OS2_CRT_AUTO && !beside)) && ldcres % 16 == 0 &&
          (reinterpret_cast<uintptr_t>(c) & 15) == 0;
 }
 cudaError_t crt_launch(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
                        const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
-                       int *status, cudaStream_t s) {
-  if (crt_on_tc(ldcres, c))
+                       int *status, cudaStream_t s, bool beside = false) {
+  if (crt_on_tc(ldcres, c, beside))
     return launch_crt_tc(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, status, s);
   return launch_crt(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, s);
 }
@@ -489,8 +492,19 @@ int panel_size(int rows) {
 
 // The five steps on device operands; arguments already checked.  f32: float
 // operands and result (SGEMM emulation), else double.
+// Step 1 from exponents the caller already has (e_in for A's m rows, f_in for
+// B's n columns): copied into the workspace.
+cudaError_t given_exponents(int m, int n, const int32_t *e_in, const int32_t *f_in, void *ws,
+                            const Layout &L, cudaStream_t s) {
+  cudaError_t err = cudaMemcpyAsync(at<int32_t>(ws, L.e), e_in, 4 * (size_t)m,
+                                    cudaMemcpyDeviceToDevice, s);
+  if (err) return err;
+  return cudaMemcpyAsync(at<int32_t>(ws, L.f), f_in, 4 * (size_t)n, cudaMemcpyDeviceToDevice, s);
+}
+
 os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const void *B, int ldb,
-                    void *C, int ldc, int N, int mode, void *ws, const Layout &L, cudaStream_t s) {
+                    void *C, int ldc, int N, int mode, void *ws, const Layout &L, cudaStream_t s,
+                    const int32_t *e_in = nullptr, const int32_t *f_in = nullptr) {
   const size_t es = f32 ? 4 : 8;
   if (m == 0 || n == 0) return OS2_OK;
   if (k == 0) return cuda_status(cudaMemset2DAsync(C, (size_t)ldc * es, 0, (size_t)n * es, m, s));
@@ -501,7 +515,9 @@ os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const
   void *pa = at<void>(ws, L.planesA), *pb = at<void>(ws, L.planesB);
   int8_t *cres = at<int8_t>(ws, L.cres);
   cudaError_t err;
-  if (mode == OS2_MODE_FAST) {
+  if (e_in) {
+    if ((err = given_exponents(m, n, e_in, f_in, ws, L, s))) return cuda_status(err);
+  } else if (mode == OS2_MODE_FAST) {
     // step 1: exponents from the revised bound (A's rows and B's columns)
     ProfScope ps("scale", s);
     if ((err = launch_row_scale(SM_FAST_SCALE, f32, A, lda, m, e, nullptr, nullptr, B, ldb, n, f,
@@ -561,7 +577,8 @@ DevPipe *dev_pipe() {
 // results are those of run_gemm: every entry goes through the same steps.
 os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
                            int ldb, void *C, int ldc, int N, int mode, void *ws, const Layout &L,
-                           cudaStream_t s) {
+                           cudaStream_t s, const int32_t *e_in = nullptr,
+                           const int32_t *f_in = nullptr) {
   const size_t es = f32 ? 4 : 8;
   const Os2Tables *t = os2_tables(N);
   int *status = os2_status_ptr();
@@ -583,7 +600,9 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
     if ((err = (x)) != cudaSuccess) return cuda_status(err); \
   } while (0)
   // step 1 on `stream`
-  if (mode == OS2_MODE_FAST) {
+  if (e_in) {
+    OS2_TRY(given_exponents(m, n, e_in, f_in, ws, L, s));
+  } else if (mode == OS2_MODE_FAST) {
     ProfScope ps("scale", s);
     OS2_TRY(launch_row_scale(SM_FAST_SCALE, f32, A, lda, m, e, nullptr, nullptr, B, ldb, n, f,
                              nullptr, nullptr, k, L.kp, t, status, s));
@@ -613,7 +632,7 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
     OS2_TRY(cudaStreamWaitEvent(p->crt, p->g_done[i], 0));
     ProfScope ps("crt_unscale", p->crt);
     OS2_TRY(crt_launch(f32, mi, n, ci, L.ldcres, e + r0, f, Cb + (size_t)r0 * ldc * es, ldc,
-                       nullptr, t, status, p->crt));
+                       nullptr, t, status, p->crt, true));
   }
   // `stream` covers everything: it waits for the last reconstruction
   OS2_TRY(cudaEventRecord(p->done, p->crt));
@@ -626,15 +645,18 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
 // product leaves idle.  The tensor-core CRT needs TMEM and more shared memory
 // than a product CTA leaves free, so it cannot run beside a product: with it
 // the five steps run in one pass (one product launch, no panel tails).
+// Measured at 8192^3 the two plans tie at 16 moduli, and the panels win at 18
+// (the tensor-core CRT then takes 1.0 ms in series), so AUTO takes panels.
 bool use_panels(int m) { return panel_size(m) < m && g_crt_variant.load() != OS2_CRT_TC; }
 
 // run_gemm_panels when A has more than one row panel, else run_gemm.
 os2_status run_gemm_auto(bool f32, int m, int n, int k, const void *A, int lda, const void *B,
                          int ldb, void *C, int ldc, int N, int mode, void *ws, const Layout &L,
-                         cudaStream_t s) {
+                         cudaStream_t s, const int32_t *e_in = nullptr,
+                         const int32_t *f_in = nullptr) {
   if (m > 0 && n > 0 && k > 0 && use_panels(m))
-    return run_gemm_panels(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s);
-  return run_gemm(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s);
+    return run_gemm_panels(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s, e_in, f_in);
+  return run_gemm(f32, m, n, k, A, lda, B, ldb, C, ldc, N, mode, ws, L, s, e_in, f_in);
 }
 
 }  // namespace
@@ -948,7 +970,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
     // next block's product; the tensor-core one follows the product on `stream`
     cudaEvent_t gd = p->g_done[blocks], done = p->c_done[blocks];
     blocks++;
-    const bool tc = crt_on_tc(L.ldcres, ci);
+    const bool tc = crt_on_tc(L.ldcres, ci, true);
     cudaStream_t cs = tc ? s : p->crt;
     if (!tc) {
       if ((err = cudaEventRecord(gd, s))) return cuda_status(err);
@@ -1030,6 +1052,65 @@ os2_status os2_scale(int m, int n, int k, const double *A, int lda, const double
     return cuda_status(err);
   if ((err = launch_accu_exponents(R, EA, m, e, t, s))) return cuda_status(err);
   return cuda_status(launch_accu_exponents(K, EB, n, f, t, s));
+}
+
+os2_status os2_scale_bounds(int m, int n, int k, const double *A, int lda, const double *B,
+                            int ldb, int32_t *R, int32_t *K, int32_t *EA, int32_t *EB,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  if (m < 0 || n < 0 || k < 0) return OS2_ERR_INVALID_ARG;
+  if (lda < std::max(k, 1) || ldb < std::max(k, 1)) return OS2_ERR_INVALID_ARG;
+  if (k >= kMaxKAccurate) return OS2_ERR_UNSUPPORTED;
+  if ((m && (!R || !EA || (k && !A))) || (n && (!K || !EB || (k && !B)))) return OS2_ERR_INVALID_ARG;
+  if ((A && !aligned(A, 8)) || (B && !aligned(B, 8))) return OS2_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Os2Tables *t = os2_tables(1);
+  int *status = os2_status_ptr();
+  if (!t || !status) return OS2_ERR_CUDA;
+  cudaError_t err;
+  if (m && (err = cudaMemsetAsync(R, 0, 4 * (size_t)m, s))) return cuda_status(err);
+  if (n && (err = cudaMemsetAsync(K, 0, 4 * (size_t)n, s))) return cuda_status(err);
+  if (k == 0) {  // every row is zero: E = 0, bound 0
+    if (m && (err = cudaMemsetAsync(EA, 0, 4 * (size_t)m, s))) return cuda_status(err);
+    if (n && (err = cudaMemsetAsync(EB, 0, 4 * (size_t)n, s))) return cuda_status(err);
+    return OS2_OK;
+  }
+  Layout L;
+  make_layout(m, n, k, 1, OS2_MODE_ACCURATE, &L);
+  if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return OS2_ERR_WORKSPACE;
+  void *pa = at<void>(workspace, L.planesA), *pb = at<void>(workspace, L.planesB);
+  if ((err = launch_row_scale(SM_BARS, false, A, lda, m, nullptr, EA, pa, B, ldb, n, nullptr, EB,
+                              pb, k, L.kp, t, status, s)))
+    return cuda_status(err);
+  if (m > 0 && n > 0 && (err = bound_product(m, n, L, workspace, pa, pb, R, K, t, status, s)))
+    return cuda_status(err);
+  return OS2_OK;
+}
+
+os2_status os2_exponents_from_bounds(int count, const int32_t *bound, const int32_t *E,
+                                     int num_moduli, int32_t *e, void *stream) {
+  if (count < 0 || num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
+  if (count == 0) return OS2_OK;
+  if (!bound || !E || !e) return OS2_ERR_INVALID_ARG;
+  const Os2Tables *t = os2_tables(num_moduli);
+  if (!t) return OS2_ERR_CUDA;
+  return cuda_status(launch_accu_exponents(bound, E, count, e, t, static_cast<cudaStream_t>(stream)));
+}
+
+os2_status os2_gemm_exponents(int m, int n, int k, const double *A, int lda, const double *B,
+                              int ldb, double *C, int ldc, int num_moduli, const int32_t *e,
+                              const int32_t *f, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+  os2_status st = check_gemm_args(m, n, k, A, lda, B, ldb, C, ldc, num_moduli, OS2_MODE_FAST);
+  if (st) return st;
+  if ((m > 0 && !e) || (n > 0 && !f)) return OS2_ERR_INVALID_ARG;
+  Layout L;
+  make_layout(m, n, k, num_moduli, OS2_MODE_FAST, &L);
+  if (m > 0 && n > 0 && k > 0) {
+    if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256))
+      return OS2_ERR_WORKSPACE;
+  }
+  return run_gemm_auto(false, m, n, k, A, lda, B, ldb, C, ldc, num_moduli, OS2_MODE_FAST,
+                       workspace, L, static_cast<cudaStream_t>(stream), e, f);
 }
 
 os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t *exps,
@@ -1136,7 +1217,8 @@ os2_status os2_peak_probe(int kind, int iters, int check, int32_t *result, doubl
 }
 
 os2_status os2_set_crt_variant(int variant) {
-  if (variant != OS2_CRT_TC && variant != OS2_CRT_SIMT) return OS2_ERR_INVALID_ARG;
+  if (variant != OS2_CRT_TC && variant != OS2_CRT_SIMT && variant != OS2_CRT_AUTO)
+    return OS2_ERR_INVALID_ARG;
   g_crt_variant.store(variant);
   return OS2_OK;
 }

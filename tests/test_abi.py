@@ -58,21 +58,23 @@ def test_workspace_sizes():
     assert h >= os2.workspace_size(64, 64, 64, 14) + 3 * 64 * 64 * 8
     assert os2.launch_count(64, 64, 64, 14, "fast") == 4
     assert os2.launch_count(64, 64, 64, 14, "accurate") == 7
-    assert os2.launch_count(4095, 64, 64, 14, "fast") == 4
-    # tensor-core CRT (default): one pass whatever m
-    assert os2.launch_count(8192, 64, 64, 14, "fast") == 4
-    assert os2.launch_count(8192, 64, 64, 14, "accurate") == 7
-    assert os2.launch_count(8192, 64, 8192, 14, "accurate") == 3 + 2 + 3   # 2 bound segments
-    # CUDA-core CRT: row panels of about 2048 rows for m >= 4096
-    os2.set_crt_variant(os2.CRT_SIMT)
-    try:
+    # default (and CUDA-core CRT): row panels of about 2048 rows for m >= 4096
+    for v in (os2.CRT_AUTO, os2.CRT_SIMT):
+        os2.set_crt_variant(v)
         assert os2.launch_count(4095, 64, 64, 14, "fast") == 4          # one row panel
         assert os2.launch_count(8192, 64, 64, 14, "fast") == 1 + 3 * 4   # four row panels
         assert os2.launch_count(8192, 64, 64, 14, "accurate") == 4 + 3 * 4
         assert os2.launch_count(8192, 64, 8192, 14, "accurate") == 3 + 2 + 3 * 4
+    # tensor-core CRT: one pass whatever m
+    os2.set_crt_variant(os2.CRT_TC)
+    try:
+        assert os2.launch_count(4095, 64, 64, 14, "fast") == 4
+        assert os2.launch_count(8192, 64, 64, 14, "fast") == 4
+        assert os2.launch_count(8192, 64, 64, 14, "accurate") == 7
+        assert os2.launch_count(8192, 64, 8192, 14, "accurate") == 3 + 2 + 3   # 2 bound segments
     finally:
-        os2.set_crt_variant(os2.CRT_TC)
-    assert os2.load().os2_set_crt_variant(2) == 1
+        os2.set_crt_variant(os2.CRT_AUTO)
+    assert os2.load().os2_set_crt_variant(3) == 1
 
 
 def test_argument_errors_are_synchronous():

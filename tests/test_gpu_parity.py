@@ -38,13 +38,15 @@ def check_tolerance(C, A, Bt, rows, cols, ref):
     assert np.all(np.abs(C - ref) <= TOL * absprod)
 
 
-@pytest.fixture(params=[os2.CRT_TC, os2.CRT_SIMT], ids=["crt_tc", "crt_simt"])
+@pytest.fixture(params=[os2.CRT_TC, os2.CRT_SIMT, os2.CRT_AUTO],
+                ids=["crt_tc", "crt_simt", "crt_auto"])
 def crt_variant(request):
-    """Runs a test with each kernel of steps 4 + 5 (tensor-core limb sums and
-    CUDA-core multiply-adds); both must give the oracle's bits."""
+    """Runs a test with each choice of the kernel of steps 4 + 5 (tensor-core
+    limb sums, CUDA-core multiply-adds, and the default mix of the two); all
+    must give the oracle's bits."""
     os2.set_crt_variant(request.param)
     yield request.param
-    os2.set_crt_variant(os2.CRT_TC)
+    os2.set_crt_variant(os2.CRT_AUTO)
 
 
 SHAPES = [(64, 64, 64), (1, 1, 1), (3, 5, 7), (129, 257, 65), (300, 520, 1000), (128, 256, 960),
