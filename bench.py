@@ -63,6 +63,9 @@ def parse():
                     help="skip the tensor-pipe peak probes (own kernels) before the timed steps")
     ap.add_argument("--crt", default="default", choices=["default", "tc", "simt", "auto"],
                     help="kernel of steps 4 + 5 (os2_set_crt_variant); default: the library's")
+    ap.add_argument("--gemm", default="tc", choices=["tc", "tc_1sm", "tc_i8", "simt"],
+                    help="step-3 kernel (os2_set_gemm_variant): tc (default), tc_1sm, tc_i8 "
+                         "(int8 residue planes widened on chip) or simt")
     ap.add_argument("--accuracy", action="store_true",
                     help="error against the exact product for 1024^3, phi in {0.5,2,4}, N in "
                          "{12..20}, both modes, beside native DGEMM; prints one JSON line")
@@ -330,6 +333,8 @@ def run_ours(a):
     import rns_emulated_fp64_gb300 as os2
     world, rank, local = dist_setup(a)
     dev = torch.device("cuda", local if world > 1 else 0)
+    os2.set_gemm_variant({"tc": os2.GEMM_TC, "tc_1sm": os2.GEMM_TC_1SM, "tc_i8": os2.GEMM_TC_I8,
+                          "simt": os2.GEMM_SIMT}[a.gemm])
     if a.crt != "default":
         os2.set_crt_variant({"tc": os2.CRT_TC, "simt": os2.CRT_SIMT, "auto": os2.CRT_AUTO}[a.crt])
     m, n, k, N = a.m, a.n, a.k, a.num_moduli
@@ -432,7 +437,7 @@ def run_ours(a):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_max / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config(a, {"crt_kernel": a.crt}), "clocks": clk,
+            "config": config(a, {"crt_kernel": a.crt, "gemm_kernel": a.gemm}), "clocks": clk,
             "gpu_launches": os2.launch_count(m, n, k, N, a.mode) * a.steps,
             "roofline": roofline, "kernels": kern}
     if peaks_probe:

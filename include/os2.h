@@ -73,7 +73,11 @@ typedef enum {
 typedef enum {
   OS2_GEMM_TC = 0,        /* tcgen05 2-SM tensor-core kernel, 256x256 tiles (default) */
   OS2_GEMM_SIMT = 1,      /* plain CUDA-core int32 kernel (exact reference, slow) */
-  OS2_GEMM_TC_1SM = 2     /* tcgen05 single-SM tensor-core kernel, 128x256 tiles */
+  OS2_GEMM_TC_1SM = 2,    /* tcgen05 single-SM tensor-core kernel, 128x256 tiles */
+  OS2_GEMM_TC_I8 = 3      /* as OS2_GEMM_TC, from int8 residue planes in HBM (half the
+                             bytes of FP16) widened to FP16 on chip by four extra warps;
+                             step 2 then writes int8 planes (os2_gemm, os2_gemm_host,
+                             os2_sgemm, complex products; not os2_gemm_residues) */
 } os2_gemm_variant;
 
 typedef enum {
@@ -286,7 +290,8 @@ os2_status os2_wait_selftest(long long limit_cycles, int32_t *result, void *stre
  * OS2_ERR_INVALID_ARG for another value. */
 os2_status os2_set_crt_variant(int variant);
 
-/* Selects the step-3 kernel used by os2_gemm (process-wide; default TC). */
+/* Selects the step-3 kernel used by os2_gemm and the other whole-path entry
+ * points (process-wide; default OS2_GEMM_TC).  All give identical results. */
 os2_status os2_set_gemm_variant(int variant);
 
 /* Static description of a status code. */

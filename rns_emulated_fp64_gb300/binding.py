@@ -17,7 +17,7 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, 1, 2, 3
 ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA = 4, 5, 6, 7
 MODE_FAST, MODE_ACCURATE = 0, 1
-GEMM_TC, GEMM_SIMT, GEMM_TC_1SM = 0, 1, 2
+GEMM_TC, GEMM_SIMT, GEMM_TC_1SM, GEMM_TC_I8 = 0, 1, 2, 3
 CRT_TC, CRT_SIMT, CRT_AUTO = 0, 1, 2
 OUT_MODP_INT8, OUT_RAW_INT32 = 0, 1
 KP_ALIGN, CRES_ALIGN = 64, 16

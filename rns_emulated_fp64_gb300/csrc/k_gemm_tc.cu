@@ -522,14 +522,49 @@ __device__ __forceinline__ void bound_epilogue(uint32_t taddr, int grow, int col
   if (bs.last && row_ok) atomicMax(&bs.rowmax[grow], rmax);
 }
 
-template <int BOUND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// int8-plane variant (I8 = 1): the residue planes come from HBM as int8 (half
+// the bytes of FP16); TMA copies each CTA's 128 rows x 128 k of A and of B into
+// a ring of int8 stages (unswizzled 128-byte rows, completion on the CTA's own
+// barrier), and four more warps widen a stage into the FP16 operand ring the
+// MMAs read (same 128-byte-swizzled layout as the TMA writes in the FP16
+// kernel): 1024 + (r + 128) is the FP16 with bit pattern 0x64 followed by the
+// byte r ^ 0x80, and one packed FP16 add of -1152 leaves r exactly.  Both CTAs'
+// converters (eight warps each) arrive on the even CTA's "operand full"
+// barrier; the MMA's commit is multicast to both CTAs' "operand empty"
+// barriers as before.
+constexpr int kStages2I8 = 2;      // FP16 operand stages of the int8 variant
+constexpr int kRawStages2 = 3;     // int8 stages
+constexpr int kConvThreads = 256;  // converter warps 6-13
+
+template <int I8>
+constexpr size_t smem2_bytes() {
+  return 1024 + (size_t)(I8 ? kStages2I8 : kStages2) * 2 * 2 * kHalf * BK * 2 +
+         (I8 ? (size_t)kRawStages2 * 2 * kHalf * BK2 : 0) + 256;
+}
+
+__device__ __forceinline__ uint32_t hadd2_bits(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Exact FP16 of the four int8 residues of a word: [r0 r1] and [r2 r3].
+__device__ __forceinline__ void widen_exact(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  lo = hadd2_bits(__byte_perm(x, 0x64646464u, 0x4140), 0xE480E480u);  // - 1152
+  hi = hadd2_bits(__byte_perm(x, 0x64646464u, 0x4342), 0xE480E480u);
+}
+
+template <int BOUND, int I8 = 0>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(I8 ? kThreads + kConvThreads : kThreads, 1)
     k_gemm_tc2(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                const Sched sp, const GemmConsts gc, int8_t *__restrict__ out, int ldo,
                const BoundSeg bs, int *status) {
-  constexpr int BN = 256, STAGES = kStages2;
+  constexpr int BN = 256, STAGES = I8 ? kStages2I8 : kStages2;
+  constexpr int RSTAGES = I8 ? kRawStages2 : 0;
   constexpr uint32_t HALF = kHalf * BK * 2;  // one k-block of 128 rows
   constexpr uint32_t A_BYTES = 2 * HALF, B_BYTES = 2 * HALF;
+  constexpr uint32_t RAW_HALF = kHalf * BK2;  // int8 stage: 128 rows x 128 bytes of A (or B)
+  constexpr uint32_t RAW_BYTES = 2 * RAW_HALF;
   constexpr uint32_t IDESC = idesc_f16_f32(2 * kHalf, BN);
   constexpr uint32_t TMEM_COLS = 512;
 
@@ -538,10 +573,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                               ~uintptr_t(1023));
   uint8_t *sA = smem;
   uint8_t *sB = smem + STAGES * A_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+  uint8_t *sRaw = sB + STAGES * B_BYTES;  // int8 stages (I8)
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sRaw + RSTAGES * RAW_BYTES);
   uint64_t *full = bars, *empty = bars + STAGES;
   uint64_t *acc_full = bars + 2 * STAGES, *acc_empty = acc_full + 2, *mma_done = acc_empty + 2;
-  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(mma_done + 1);
+  uint64_t *rfull = mma_done + 1, *rempty = rfull + RSTAGES;  // int8 ring (I8)
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(rempty + RSTAGES);
   volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -551,8 +588,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; s++) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], I8 ? 2 * kConvThreads : 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < RSTAGES; s++) {
+      mbar_init(&rfull[s], 1);
+      mbar_init(&rempty[s], kConvThreads);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&acc_full[b], 1);
@@ -576,7 +617,109 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
 
-  if (warp == 0) {
+  if (I8 && warp == 0) {
+    // ------------------------------------------------------------ int8 copies
+    if (lane == 0) {
+      int rs = 0;
+      uint32_t rph = 0, used = 0, last_par = 0;
+      for_each_unit_of<0>(sp, pair, npairs, [&](int job, int c, int) -> bool {
+        int l, tm, tn;
+        job_coords(job, sp, l, tm, tn);
+        const int kb0 = chunk_begin(sp, c), kb1 = chunk_begin(sp, c + 1);
+        for (int kb = kb0; kb < kb1; kb++) {
+          if (!mbar_wait_bounded(&rempty[rs], rph ^ 1, s_abort, kWaitLimit)) {
+            *s_abort = 1;
+            set_status(status, OS2_ERR_TIMEOUT);
+            return false;
+          }
+          mbar_arrive_expect_tx(&rfull[rs], RAW_BYTES);
+          // a stage past the last k-block reads zeros (out-of-range box)
+          tma_load_3d(sRaw + rs * RAW_BYTES, &mapA, &rfull[rs], kb * BK2,
+                      tm * 2 * kHalf + (int)rank * kHalf, l);
+          tma_load_3d(sRaw + rs * RAW_BYTES + RAW_HALF, &mapB, &rfull[rs], kb * BK2,
+                      tn * BN + (int)rank * kHalf, l);
+          used |= 1u << rs;
+          last_par = (last_par & ~(1u << rs)) | (rph << rs);
+          if (++rs == RSTAGES) {
+            rs = 0;
+            rph ^= 1;
+          }
+        }
+        return true;
+      });
+      for (int s = 0; s < RSTAGES; s++)
+        if (used >> s & 1) {
+          volatile int no_abort = 0;
+          mbar_wait_bounded(&rfull[s], (last_par >> s) & 1, &no_abort, kWaitLimit);
+        }
+    }
+  } else if (I8 && warp >= 2 + kEpiThreads / 32) {
+    // ------------------------------------------------------------ int8 -> FP16
+    // thread ct widens 16-byte chunks q = ct + 256 i of the stage (A's 1024
+    // chunks, then B's): the 8 lanes of a quarter-warp take the 8 chunks of one
+    // 128-byte row, and each chunk becomes two 16-byte FP16 chunks of k-block
+    // (chunk / 4) of the swizzled operand tile
+    const int ct = threadIdx.x - kThreads;
+    uint32_t full_leader[STAGES];
+#pragma unroll
+    for (int s2 = 0; s2 < STAGES; s2++) full_leader[s2] = mapa_shared(smem_u32(&full[s2]), 0);
+    int rs = 0, fs = 0;
+    uint32_t rph = 0, fph = 0;
+    for_each_unit_of<0>(sp, pair, npairs, [&](int, int c, int) -> bool {
+      const int kb0 = chunk_begin(sp, c), kb1 = chunk_begin(sp, c + 1);
+      for (int kb = kb0; kb < kb1; kb++) {
+        const bool ok =
+            mbar_wait_bounded(&rfull[rs], rph, s_abort, kWaitLimit) &&
+            mbar_wait_cluster_bounded(&empty[fs], fph ^ 1, s_abort, kWaitLimit);
+        if (!ok) {
+          *s_abort = 1;
+          set_status(status, OS2_ERR_TIMEOUT);
+          return false;
+        }
+        const uint32_t rbase = smem_u32(sRaw + rs * RAW_BYTES);
+        const uint32_t abase = smem_u32(sA + fs * A_BYTES), bbase = smem_u32(sB + fs * B_BYTES);
+#pragma unroll
+        for (int i = 0; i < (int)(RAW_BYTES / 16) / kConvThreads; i++) {
+          const int q = i * kConvThreads + ct;
+          const int op = q >> 10, row = (q >> 3) & 127, cc = q & 7;
+          uint4 w;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                       : "r"(rbase + op * RAW_HALF + row * 128 + cc * 16));
+          uint32_t h[8];
+          widen_exact(w.x, h[0], h[1]);
+          widen_exact(w.y, h[2], h[3]);
+          widen_exact(w.z, h[4], h[5]);
+          widen_exact(w.w, h[6], h[7]);
+          const uint32_t rowa = (op ? bbase : abase) + (cc >> 2) * HALF + (row >> 3) * 1024 +
+                                (row & 7) * 128;
+          const int j0 = 2 * (cc & 3);
+          const uint32_t d0 = rowa + ((j0 ^ (row & 7)) << 4);
+          const uint32_t d1 = rowa + (((j0 + 1) ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d0), "r"(h[0]), "r"(h[1]),
+                       "r"(h[2]), "r"(h[3])
+                       : "memory");
+          asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(d1), "r"(h[4]), "r"(h[5]),
+                       "r"(h[6]), "r"(h[7])
+                       : "memory");
+        }
+        // the FP16 stage, written through the generic proxy, is read by the
+        // tensor cores of the pair
+        asm volatile("fence.proxy.async;" ::: "memory");
+        mbar_arrive_cluster(full_leader[fs]);
+        mbar_arrive(&rempty[rs]);
+        if (++rs == RSTAGES) {
+          rs = 0;
+          rph ^= 1;
+        }
+        if (++fs == STAGES) {
+          fs = 0;
+          fph ^= 1;
+        }
+      }
+      return true;
+    });
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producers
     if (lane == 0) {
       int stage = 0;
@@ -826,16 +969,33 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
   return cudaGetLastError();
 }
 
-template <int BOUND>
+template <int BOUND, int I8 = 0>
 cudaError_t set_smem2() {
-  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * 2 * kHalf * BK * 2 + 256;
+  constexpr size_t smem = smem2_bytes<I8>();
+  static_assert(smem <= 227 * 1024, "shared memory of the 2-SM kernel");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_gemm_tc2<BOUND>,
+    attr_err = cudaFuncSetAttribute(k_gemm_tc2<BOUND, I8>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
   return attr_err;
+}
+
+// int8 planes [nplanes][plane_rows][kp] bytes, of which the first `rows` rows
+// are mapped; box = 128 (k) x 128 rows x 1, no swizzle.
+bool make_map_i8(CUtensorMap *map, const void *base, int kp, int rows, int nplanes,
+                 int plane_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kp, (cuuint64_t)rows, (cuuint64_t)nplanes};
+  cuuint64_t strides[2] = {(cuuint64_t)kp, (cuuint64_t)kp * (cuuint64_t)plane_rows};
+  cuuint32_t box[3] = {(cuuint32_t)BK2, (cuuint32_t)kHalf, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 Sched sched2(int m, int n, int kb_total, int nplanes) {
@@ -850,15 +1010,19 @@ Sched sched2(int m, int n, int kb_total, int nplanes) {
   return sp;
 }
 
+// i8: RA, RB are int8 planes (the int8-plane variant), else FP16 planes.
 cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
-                    int ldo, const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows) {
-  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * 2 * kHalf * BK * 2 + 256;
-  cudaError_t attr_err = set_smem2<0>();
+                    int ldo, const Os2Tables *t, int *status, cudaStream_t s, int b_plane_rows,
+                    bool i8 = false) {
+  const size_t smem = i8 ? smem2_bytes<1>() : smem2_bytes<0>();
+  cudaError_t attr_err = i8 ? set_smem2<0, 1>() : set_smem2<0>();
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, RA, kp, m, nplanes, kHalf, m) ||
-      !make_map(&mb, RB, kp, n, nplanes, kHalf, b_plane_rows))
-    return cudaErrorInvalidValue;
+  const bool maps = i8 ? make_map_i8(&ma, RA, kp, m, nplanes, m) &&
+                             make_map_i8(&mb, RB, kp, n, nplanes, b_plane_rows)
+                       : make_map(&ma, RA, kp, m, nplanes, kHalf, m) &&
+                             make_map(&mb, RB, kp, n, nplanes, kHalf, b_plane_rows);
+  if (!maps) return cudaErrorInvalidValue;
   // the 2-SM kernel counts k in stages of two k-blocks
   Sched sp = sched2(m, n, (kp / BK + 1) / 2, nplanes);
   sp.chunk = (int)(((1LL << 24) - 135) / ((long long)BK2 << 14));
@@ -866,8 +1030,13 @@ cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int np
   if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
   const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
   GemmConsts gc = t ? t->gemm : GemmConsts{};
-  k_gemm_tc2<0><<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, gc, reinterpret_cast<int8_t *>(out),
-                                                  ldo, BoundSeg{}, status);
+  if (i8)
+    k_gemm_tc2<0, 1><<<2 * pairs, kThreads + kConvThreads, smem, s>>>(
+        ma, mb, sp, gc, reinterpret_cast<int8_t *>(out), ldo, BoundSeg{}, status);
+  else
+    k_gemm_tc2<0><<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, gc,
+                                                    reinterpret_cast<int8_t *>(out), ldo,
+                                                    BoundSeg{}, status);
   return cudaGetLastError();
 }
 
@@ -876,7 +1045,7 @@ cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int np
 cudaError_t launch2_bound(int m, int n, int kp, const void *RA, const void *RB, int32_t *partial,
                           int ldp, int32_t *rowmax, int32_t *colmax, int *status,
                           cudaStream_t s) {
-  constexpr size_t smem = 1024 + (size_t)kStages2 * 2 * 2 * kHalf * BK * 2 + 256;
+  constexpr size_t smem = smem2_bytes<0>();
   constexpr int kSegMax = (int)((1LL << 24) / ((long long)BK2 << 12));  // 32 stages, 4096 terms
   cudaError_t attr_err = set_smem2<1>();
   if (attr_err != cudaSuccess) return attr_err;
@@ -914,6 +1083,8 @@ cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const
   if (b_plane_rows <= 0) b_plane_rows = n;
   if (b_plane_rows < n) return cudaErrorInvalidValue;
   if (kind == 2) return launch2(m, n, kp, RA, RB, nplanes, out, ldo, t, status, s, b_plane_rows);
+  if (kind == 3)
+    return launch2(m, n, kp, RA, RB, nplanes, out, ldo, t, status, s, b_plane_rows, true);
   if (kind == 0)
     return launch<0>(m, n, kp, RA, RB, nplanes, out, ldo, rowmax, colmax, prod_bound_log2, t,
                      status, s, b_plane_rows);

@@ -95,8 +95,27 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigne
   return d;
 }
 
+// EPT residues (exact small integers held as floats) as int8: the low byte of
+// r + 1.5 * 2^23 is r in two's complement.
+template <int EPT>
+__device__ __forceinline__ void store_i8(const float (&r)[EPT], int8_t *dst) {
+  uint32_t b[EPT];
+#pragma unroll
+  for (int u = 0; u < EPT; u++) b[u] = __float_as_uint(r[u] + 12582912.0f);
+  uint32_t w[EPT / 4];
+#pragma unroll
+  for (int q = 0; q < EPT / 4; q++)
+    w[q] = __byte_perm(__byte_perm(b[4 * q], b[4 * q + 1], 0x0040),
+                       __byte_perm(b[4 * q + 2], b[4 * q + 3], 0x0040), 0x5410);
+  if (EPT == 8)
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[EPT == 8 ? 1 : 0]);
+  else
+    *reinterpret_cast<uint32_t *>(dst) = w[0];
+}
+
 // Residues of EPT entries (held as int_words gives them) for every modulus,
-// one vector store of EPT FP16 values per plane.  For odd p_l, with
+// one vector store of EPT values per plane: FP16 (exact for |r| <= 2048), or
+// int8 when `i8` (half the bytes; the step-3 variant widens them on chip).  For odd p_l, with
 // c_t = 2^(15t) mod p_l and K = 2^14 (c_0 + ... + c_(NW-2)) mod p_l, both held
 // around zero: x = K + sum_t w_t c_t is congruent to the integer, and for the
 // twenty moduli of the set and NW <= 6, |x| <= 2^14 sum_t |c_t| + |K| <
@@ -107,10 +126,16 @@ __device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigne
 // go through each packed instruction.
 template <int N, int NW, int EPT>
 __device__ __forceinline__ void emit(const float (&w)[EPT][NW], const uint32_t (&lb)[EPT],
-                                     const ResConsts &c, __half *dst, size_t pstride) {
+                                     const ResConsts &c, __half *dst, size_t pstride, bool i8) {
   static_assert(EPT == 4 || EPT == 8, "4 or 8 entries per thread");
   using Vec = typename std::conditional<EPT == 8, uint4, uint2>::type;
-  {
+  int8_t *dst8 = reinterpret_cast<int8_t *>(dst);  // int8 planes: element offsets in bytes
+  if (i8) {
+    float r[EPT];
+#pragma unroll
+    for (int u = 0; u < EPT; u++) r[u] = byte_residue(lb[u]);
+    store_i8<EPT>(r, dst8);
+  } else {
     __align__(16) __half2 v[EPT / 2];
 #pragma unroll
     for (int u = 0; u < EPT / 2; u++)
@@ -126,24 +151,29 @@ __device__ __forceinline__ void emit(const float (&w)[EPT][NW], const uint32_t (
   constexpr unsigned long long kNegMagic2 = 0xCB400000CB400000ull;  // -1.5 * 2^23, twice
 #pragma unroll
   for (int l = 1; l < N; l++) {
-    __align__(16) __half2 v[EPT / 2];
+    float r[EPT];
 #pragma unroll
     for (int u = 0; u < EPT / 2; u++) {
       unsigned long long x = fma2(W[u][0], c.w15x2[l][0], c.k15x2[l][NW - 4]);
 #pragma unroll
       for (int t = 1; t < NW; t++) x = fma2(W[u][t], c.w15x2[l][t], x);
       const unsigned long long q = add2(fma2(x, c.invp2[l], kMagic2), kNegMagic2);
-      float r0, r1;
-      unpack2(fma2(c.negp2[l], q, x), r0, r1);
-      v[u] = __floats2half2_rn(r0, r1);
+      unpack2(fma2(c.negp2[l], q, x), r[2 * u], r[2 * u + 1]);
     }
-    *reinterpret_cast<Vec *>(dst + l * pstride) = *reinterpret_cast<Vec *>(v);
+    if (i8) {
+      store_i8<EPT>(r, dst8 + l * pstride);
+    } else {
+      __align__(16) __half2 v[EPT / 2];
+#pragma unroll
+      for (int u = 0; u < EPT / 2; u++) v[u] = __floats2half2_rn(r[2 * u], r[2 * u + 1]);
+      *reinterpret_cast<Vec *>(dst + l * pstride) = *reinterpret_cast<Vec *>(v);
+    }
   }
 }
 
 template <int N, int NW, typename T, int EPT>
 __device__ __forceinline__ void residues_of(const T (&v)[EPT], int ee, const ResConsts &c,
-                                            __half *dst, size_t pstride) {
+                                            __half *dst, size_t pstride, bool i8) {
   float w[EPT][NW];
   uint32_t lb[EPT];
 #pragma unroll
@@ -151,7 +181,7 @@ __device__ __forceinline__ void residues_of(const T (&v)[EPT], int ee, const Res
     const Dec d = decode(v[u]);
     int_words<NW>(d, d.ex2 + ee, w[u], lb[u]);
   }
-  emit<N, NW, EPT>(w, lb, c, dst, pstride);
+  emit<N, NW, EPT>(w, lb, c, dst, pstride, i8);
 }
 
 // Residue planes: EPT consecutive entries per thread, one vector store per plane.
@@ -159,7 +189,8 @@ constexpr int kEPT = 8;
 
 template <int N, typename T>
 __global__ void __launch_bounds__(kThreads, 3)
-    k_residues(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status) {
+    k_residues(const RowSet a, const RowSet b, int k, int kp, const ResConsts c, int *status,
+               bool i8) {
   constexpr int EPT = kEPT;
   const int cpr = kp / EPT;  // chunks per row
   const int total_rows = a.rows + b.rows;
@@ -188,13 +219,16 @@ __global__ void __launch_bounds__(kThreads, 3)
         const Dec d = decode(v[u]);
         if (d.mant) top = max(top, d.ex2 + 64 - __clzll((long long)d.mant) + ee);
       }
-      __half *dst = rs.planes + (size_t)row * kp + h0;
+      // element offset row * kp + h0 (FP16 or int8 elements)
+      __half *dst = i8 ? reinterpret_cast<__half *>(reinterpret_cast<int8_t *>(rs.planes) +
+                                                     (size_t)row * kp + h0)
+                       : rs.planes + (size_t)row * kp + h0;
       if (top <= 59) {
-        residues_of<N, 4>(v, ee, c, dst, pstride);
+        residues_of<N, 4>(v, ee, c, dst, pstride, i8);
       } else if (top <= 74) {
-        residues_of<N, 5>(v, ee, c, dst, pstride);
+        residues_of<N, 5>(v, ee, c, dst, pstride, i8);
       } else if (top <= 89) {
-        residues_of<N, 6>(v, ee, c, dst, pstride);
+        residues_of<N, 6>(v, ee, c, dst, pstride, i8);
       } else {
         // beyond every exponent that step 1 produces (|integer| < 2^84):
         // reported, and the entries' residues are left as zero
@@ -202,7 +236,12 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int l = 0; l < N; l++)
 #pragma unroll
-          for (int u = 0; u < EPT; u++) dst[l * pstride + u] = __float2half(0.0f);
+          for (int u = 0; u < EPT; u++) {
+            if (i8)
+              reinterpret_cast<int8_t *>(dst)[l * pstride + u] = 0;
+            else
+              dst[l * pstride + u] = __float2half(0.0f);
+          }
       }
     }
   }
@@ -210,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 3)
 
 template <int N, typename T>
 cudaError_t residues_launch(const RowSet &a, const RowSet &b, int k, int kp, const ResConsts &c,
-                            int *status, cudaStream_t s) {
+                            int *status, cudaStream_t s, bool i8) {
   const int cpr = kp / kEPT;
   const int bx = (cpr + kThreads - 1) / kThreads;
   const int rows = a.rows + b.rows;
   dim3 grid(bx, rows < 65535 ? rows : 65535);
-  k_residues<N, T><<<grid, kThreads, 0, s>>>(a, b, k, kp, c, status);
+  k_residues<N, T><<<grid, kThreads, 0, s>>>(a, b, k, kp, c, status, i8);
   return cudaGetLastError();
 }
 
@@ -223,7 +262,7 @@ cudaError_t residues_launch(const RowSet &a, const RowSet &b, int k, int kp, con
 // and float (the larger N unroll more code).
 #define OS2_RESIDUES_PART(name)                                                               \
   cudaError_t name(int N, const RowSet &a, const RowSet &b, int k, int kp, const ResConsts &c, \
-                   int *status, cudaStream_t s)
+                   int *status, cudaStream_t s, bool i8)
 OS2_RESIDUES_PART(residues_d1);
 OS2_RESIDUES_PART(residues_d2);
 OS2_RESIDUES_PART(residues_d3);
@@ -234,6 +273,6 @@ OS2_RESIDUES_PART(residues_f3);
 OS2_RESIDUES_PART(residues_f4);
 #define OS2_RESIDUES_CASE(NN, T) \
   case NN:                       \
-    return residues_launch<NN, T>(a, b, k, kp, c, status, s);
+    return residues_launch<NN, T>(a, b, k, kp, c, status, s, i8);
 
 }  // namespace os2dev

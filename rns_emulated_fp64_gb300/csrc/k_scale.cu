@@ -353,7 +353,7 @@ cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int r
 cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const int32_t *eA,
                             void *planesA, const void *XB, long ldb, int rowsB,
                             const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
-                            cudaStream_t s, long prowB) {
+                            cudaStream_t s, long prowB, bool i8) {
   if (rowsA + rowsB <= 0 || kp <= 0) return cudaSuccess;
   RowSet a{XA, lda, rowsA, const_cast<int32_t *>(eA), nullptr, reinterpret_cast<__half *>(planesA),
            rowsA};
@@ -365,15 +365,15 @@ cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const
   using namespace os2dev;
   const ResConsts &c = t->res;
   if (f32) {
-    if (N <= 12) return residues_f1(N, a, b, k, kp, c, status, s);
-    if (N <= 16) return residues_f2(N, a, b, k, kp, c, status, s);
-    if (N <= 18) return residues_f3(N, a, b, k, kp, c, status, s);
-    return residues_f4(N, a, b, k, kp, c, status, s);
+    if (N <= 12) return residues_f1(N, a, b, k, kp, c, status, s, i8);
+    if (N <= 16) return residues_f2(N, a, b, k, kp, c, status, s, i8);
+    if (N <= 18) return residues_f3(N, a, b, k, kp, c, status, s, i8);
+    return residues_f4(N, a, b, k, kp, c, status, s, i8);
   }
-  if (N <= 12) return residues_d1(N, a, b, k, kp, c, status, s);
-  if (N <= 16) return residues_d2(N, a, b, k, kp, c, status, s);
-  if (N <= 18) return residues_d3(N, a, b, k, kp, c, status, s);
-  return residues_d4(N, a, b, k, kp, c, status, s);
+  if (N <= 12) return residues_d1(N, a, b, k, kp, c, status, s, i8);
+  if (N <= 16) return residues_d2(N, a, b, k, kp, c, status, s, i8);
+  if (N <= 18) return residues_d3(N, a, b, k, kp, c, status, s, i8);
+  return residues_d4(N, a, b, k, kp, c, status, s, i8);
 }
 
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,

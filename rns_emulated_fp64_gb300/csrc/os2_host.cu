@@ -285,6 +285,9 @@ void build_tables(int N, Os2Tables *t) {
 std::atomic<int> g_variant{OS2_GEMM_TC};
 std::atomic<int> g_crt_variant{OS2_CRT_AUTO};
 
+// The int8-plane step-3 kernel reads int8 residue planes (step 2 writes them so).
+bool planes_i8() { return g_variant.load() == OS2_GEMM_TC_I8; }
+
 // Optional per-kernel timing: CUDA events recorded on the launching stream
 // around every kernel that os2_gemm enqueues (no synchronisation added).
 struct ProfRec {
@@ -421,7 +424,8 @@ os2_status check_gemm_args(int m, int n, int k, const void *A, int lda, const vo
 bool bound_on_2sm(int m, const Layout &L) {
   const int segs = (L.kp + 4095) / 4096;
   const bool room = L.total - L.cres >= 4 * (size_t)m * (size_t)L.ldcres;
-  return g_variant.load() == OS2_GEMM_TC && (segs == 1 || room);
+  const int v = g_variant.load();
+  return (v == OS2_GEMM_TC || v == OS2_GEMM_TC_I8) && (segs == 1 || room);
 }
 
 // Kernel launches of bound_product.
@@ -474,7 +478,7 @@ os2_status residue_products(int m, int n, const Layout &L, const void *pa, const
   if (variant == OS2_GEMM_SIMT)
     err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
   else
-    err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : 2, m, n, L.kp, pa, pb, N, cres,
+    err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : (variant == OS2_GEMM_TC_I8 ? 3 : 2), m, n, L.kp, pa, pb, N, cres,
                          L.ldcres, nullptr, nullptr, 14, t, status, s);
   return cuda_status(err);
 }
@@ -530,7 +534,8 @@ os2_status run_gemm(bool f32, int m, int n, int k, const void *A, int lda, const
   // step 2: residue planes of A and B
   {
     ProfScope ps("residues", s);
-    if ((err = launch_residues(f32, A, lda, m, e, pa, B, ldb, n, f, pb, k, L.kp, t, s)))
+    if ((err = launch_residues(f32, A, lda, m, e, pa, B, ldb, n, f, pb, k, L.kp, t, s, 0,
+                               planes_i8())))
       return cuda_status(err);
   }
   // step 3
@@ -591,7 +596,7 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
   char *pa = at<char>(ws, L.planesA);
   void *pb = at<void>(ws, L.planesB);
   int8_t *cres = at<int8_t>(ws, L.cres);
-  const size_t plane_row = (size_t)L.kp * 2;
+  const size_t plane_row = (size_t)L.kp * (planes_i8() ? 1 : 2);  // bytes of one plane row
   const char *Ab = static_cast<const char *>(A);
   char *Cb = static_cast<char *>(C);
   cudaError_t err;
@@ -618,7 +623,7 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
       const int r0 = i * mp, mi = std::min(mp, m - r0);
       OS2_TRY(launch_residues(f32, Ab + (size_t)r0 * lda * es, lda, mi, e + r0,
                               pa + (size_t)r0 * N * plane_row, B, ldb, i == 0 ? n : 0, f, pb, k,
-                              L.kp, t, s));
+                              L.kp, t, s, 0, planes_i8()));
     }
   }
   // step 3 per panel on `stream`; steps 4 + 5 per panel on side stream 2
@@ -874,7 +879,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
   int32_t *e = at<int32_t>(workspace, L.e), *f = at<int32_t>(workspace, L.f);
   char *pa = at<char>(workspace, L.planesA), *pb = at<char>(workspace, L.planesB);
   int8_t *cres = at<int8_t>(workspace, L.cres);
-  const size_t plane_row = (size_t)L.kp * 2;  // bytes of one row of a plane
+  const size_t plane_row = (size_t)L.kp * (planes_i8() ? 1 : 2);  // bytes of one plane row
 #define OS2_TRY(x)                                           \
   do {                                                       \
     if ((err = (x)) != cudaSuccess) return cuda_status(err); \
@@ -919,7 +924,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
     {
       ProfScope ps("residues", sp);
       r = launch_residues(false, Ai, k, mi, e + r0, pa + (size_t)r0 * N * plane_row, nullptr, 0,
-                          0, nullptr, nullptr, k, L.kp, t, sp);
+                          0, nullptr, nullptr, k, L.kp, t, sp, 0, planes_i8());
     }
     return r ? r : (side ? cudaEventRecord(p->a_split[i], sp) : cudaSuccess);
   };
@@ -938,7 +943,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
     {
       ProfScope ps("residues", sp);
       r = launch_residues(false, nullptr, 0, 0, nullptr, nullptr, Bj, k, nj, f + c0,
-                          pb + (size_t)c0 * plane_row, k, L.kp, t, sp, n);
+                          pb + (size_t)c0 * plane_row, k, L.kp, t, sp, n, planes_i8());
     }
     return r ? r : (side ? cudaEventRecord(p->b_split[j], sp) : cudaSuccess);
   };
@@ -962,7 +967,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
       if (variant == OS2_GEMM_SIMT)
         err = launch_gemm_simt(mi, nj, L.kp, pai, pbj, N, OS2_OUT_MODP_INT8, ci, L.ldcres, t, s);
       else
-        err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : 2, mi, nj, L.kp, pai, pbj, N, ci,
+        err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : (variant == OS2_GEMM_TC_I8 ? 3 : 2), mi, nj, L.kp, pai, pbj, N, ci,
                              L.ldcres, nullptr, nullptr, 14, t, status, s, n);
       if (err) return cuda_status(err);
     }
@@ -1135,7 +1140,7 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
   if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
   if (out_kind != OS2_OUT_MODP_INT8 && out_kind != OS2_OUT_RAW_INT32) return OS2_ERR_INVALID_ARG;
   if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM)
-    return OS2_ERR_INVALID_ARG;
+    return OS2_ERR_INVALID_ARG;  // (planes here are FP16; OS2_GEMM_TC_I8 reads int8 ones)
   if (ldo < std::max(n, 1)) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_MODP_INT8 && ldo % OS2_CRES_ALIGN) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_RAW_INT32 && ldo % 4) return OS2_ERR_INVALID_ARG;
@@ -1224,7 +1229,8 @@ os2_status os2_set_crt_variant(int variant) {
 }
 
 os2_status os2_set_gemm_variant(int variant) {
-  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM)
+  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM &&
+      variant != OS2_GEMM_TC_I8)
     return OS2_ERR_INVALID_ARG;
   g_variant.store(variant);
   return OS2_OK;

@@ -107,7 +107,7 @@ cudaError_t launch_row_scale(int mode, bool f32, const void *XA, long lda, int r
 cudaError_t launch_residues(bool f32, const void *XA, long lda, int rowsA, const int32_t *eA,
                             void *planesA, const void *XB, long ldb, int rowsB,
                             const int32_t *eB, void *planesB, int k, int kp, const Os2Tables *t,
-                            cudaStream_t s, long prowB = 0);
+                            cudaStream_t s, long prowB = 0, bool i8 = false);
 cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int rows, int32_t *e,
                                   const Os2Tables *t, cudaStream_t s);
 // f32: C is float (correctly rounded to binary32) instead of double.
@@ -123,7 +123,8 @@ cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *R
                              int out_kind, void *out, int ldo, const Os2Tables *t, cudaStream_t s);
 
 // tcgen05 GEMM.  kind: 0 = mod-p int8 output (single SM), 1 = exact int32 (raw
-// output and/or row/col maxima), 2 = mod-p int8 output on SM pairs (2-SM MMA).  prod_bound_log2: log2 of the largest |a*b| of one term
+// output and/or row/col maxima), 2 = mod-p int8 output on SM pairs (2-SM MMA),
+// 3 = as 2 from int8 residue planes (widened to FP16 on chip).  prod_bound_log2: log2 of the largest |a*b| of one term
 // (14 for residues, 12 for the accurate-mode magnitude planes).
 cudaError_t launch_gemm_tc(int kind, int m, int n, int kp, const void *RA, const void *RB,
                            int nplanes, void *out, int ldo, int32_t *rowmax, int32_t *colmax,

@@ -106,7 +106,9 @@ def test_argument_errors_are_synchronous():
     assert gr(4, 4, big, P, P, big, 14, 1, P, 4, 0, None) == binding.ERR_UNSUPPORTED  # raw int32 k limit
     c = lib.os2_crt
     assert c(4, 4, P, 2, 14, P, P, P, 4, None, None) == binding.ERR_INVALID_ARG     # ldcres < n
-    assert lib.os2_set_gemm_variant(3) == binding.ERR_INVALID_ARG
+    assert lib.os2_set_gemm_variant(4) == binding.ERR_INVALID_ARG
+    assert lib.os2_set_gemm_variant(binding.GEMM_TC_I8) == binding.OK
+    assert lib.os2_set_gemm_variant(binding.GEMM_TC) == binding.OK
     w = lib.os2_wait_selftest
     assert w(0, None, None) == binding.ERR_INVALID_ARG                 # limit < 1
     assert w((1 << 34) + 1, None, None) == binding.ERR_INVALID_ARG     # limit > 2^34

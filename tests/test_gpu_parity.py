@@ -314,7 +314,7 @@ def test_gemm_64cube_normal_config():
     assert_bits_equal(C, ref.C, "64^3")
 
 
-@pytest.mark.parametrize("variant", [os2.GEMM_SIMT, os2.GEMM_TC_1SM])
+@pytest.mark.parametrize("variant", [os2.GEMM_SIMT, os2.GEMM_TC_1SM, os2.GEMM_TC_I8])
 def test_gemm_variants_end_to_end(variant):
     A, Bt = workloads.make_pair("spread", 150, 170, 400, seed=1, phi=2.0)
     try:
@@ -327,6 +327,34 @@ def test_gemm_variants_end_to_end(variant):
     assert_bits_equal(Cs, Ct, "variant vs default tc")
     ref = orc.gemm_entries(A, Bt, 16, want_X=False, want_c=False, want_G=False)
     assert_bits_equal(Ct, ref.C, "tc vs oracle")
+
+
+@pytest.mark.parametrize("mode", ["fast", "accurate"])
+@pytest.mark.parametrize("m,n,k,N", [(4100, 300, 700, 16), (257, 513, 1921, 20), (3, 5, 7, 2),
+                                     (300, 260, 9000, 14)])
+def test_int8_plane_variant_oracle(mode, m, n, k, N):
+    """The int8-plane variant (step 2 writes int8 residue planes, step 3 widens
+    them to FP16 on chip): bit-exact against the oracle on a sample, with row
+    panels (m >= 4096), ragged tiles, long k (several reduction chunks) and
+    the host entry point's column panels."""
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=m + k, phi=2.0)
+    try:
+        os2.set_gemm_variant(os2.GEMM_TC_I8)
+        C = os2.gemm(dev(A), dev(Bt), N, mode).cpu().numpy()
+        status_ok()
+        Ch = torch.full((m, n), np.nan, dtype=torch.float64).pin_memory()
+        os2.gemm_host(torch.from_numpy(A).pin_memory(), torch.from_numpy(Bt).pin_memory(), Ch, N,
+                      mode)
+        torch.cuda.current_stream().synchronize()
+        status_ok()
+    finally:
+        os2.set_gemm_variant(os2.GEMM_TC)
+    rows, cols = workloads.sample_grid(m, n, 40, seed=4)
+    ref = orc.gemm_entries(A, Bt, N, rows, cols, mode=orc.FAST if mode == "fast" else orc.ACCURATE,
+                           want_X=False, want_c=False, want_G=False)
+    assert ref.mismatches == 0
+    assert_bits_equal(C[np.ix_(rows, cols)], ref.C, f"int8 planes {m}x{n}x{k} N={N} {mode}")
+    assert_bits_equal(Ch.numpy(), C, "int8 planes, host entry point vs device")
 
 
 def test_integer_inputs_exact_on_gpu():
