@@ -144,16 +144,16 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu capture, if the sources that
-    decide the kernel and its launches are unchanged since the capture (else
-    None)."""
+def kernel_traffic(kernel: str, workload_key: str):
+    """DRAM bytes per launch from a committed ncu capture, if it is for this
+    workload and the sources that decide the kernel and its launches are
+    unchanged since the capture (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as fh:
         d = json.load(fh).get(kernel)
-    if not d:
+    if not d or d.get("workload_key") != workload_key:
         return None
     if not isinstance(d.get("sources_sha256"), dict) or "bytes_per_launch" not in d:
         return None
@@ -420,7 +420,9 @@ def run_ours(a):
     if g:
         roofline = {"bound": "tensor", "kernel": "gemm_modp (tcgen05.mma kind::f16, FP16-held residues)",
                     "achieved": g["achieved"], "peak": peak_t, "unit": "TFLOP/s",
-                    "frac": g["achieved"] / peak_t, "traffic": kernel_traffic("gemm_modp"),
+                    "frac": g["achieved"] / peak_t,
+                    "traffic": (kernel_traffic("gemm_modp", f"{m}x{n}x{k}_N{N}_{a.mode}")
+                                if a.gemm == "tc" and a.crt == "default" else None),
                     "peak_source": "%s bf16 dense %s (of %s; FP16 rate = BF16 rate); timed region "
                                    "%.2f s" % (src, "sustained" if sustained else "burst", src,
                                                timed_s),
