@@ -62,7 +62,9 @@ typedef enum {
   OS2_ERR_NONFINITE = 4,    /* an input entry is Inf or NaN (device-detected) */
   OS2_ERR_RANGE = 5,        /* a scaled integer of os2_residues reached 2^89 */
   OS2_ERR_TIMEOUT = 6,      /* a device-side wait gave up (device-detected) */
-  OS2_ERR_CUDA = 7          /* a CUDA runtime/driver call failed */
+  OS2_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed */
+  OS2_ERR_BOUNDS = 8        /* debug build only: a kernel's index check failed (the access
+                               was skipped; see OS2_DEBUG in the build notes) */
 } os2_status;
 
 typedef enum {

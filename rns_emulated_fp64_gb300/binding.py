@@ -15,7 +15,7 @@ import torch
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, 1, 2, 3
-ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA = 4, 5, 6, 7
+ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA, ERR_BOUNDS = 4, 5, 6, 7, 8
 MODE_FAST, MODE_ACCURATE = 0, 1
 GEMM_TC, GEMM_SIMT, GEMM_TC_1SM, GEMM_TC_I8 = 0, 1, 2, 3
 CRT_TC, CRT_SIMT, CRT_AUTO = 0, 1, 2
@@ -42,7 +42,9 @@ class Os2Error(RuntimeError):
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The library this process loads: the in-tree build, or the path in the
+    environment variable OS2_LIB (for example the debug build)."""
+    return os.environ.get("OS2_LIB") or _build.LIB
 
 
 def load(build_if_missing: bool = True):
@@ -51,9 +53,9 @@ def load(build_if_missing: bool = True):
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB
+        path = lib_path()
         if not os.path.exists(path):
-            if not build_if_missing:
+            if not build_if_missing or path != _build.LIB:
                 raise RuntimeError(f"libos2 not built: {path} is missing")
             _build.build()
         L = ct.CDLL(path)

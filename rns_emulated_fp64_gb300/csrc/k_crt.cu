@@ -45,7 +45,7 @@ template <int N, typename OutT>
 __global__ void __launch_bounds__(kThreads)
     k_crt(int m, int n, int groups, const int8_t *__restrict__ c, int ldcres,
           const int32_t *__restrict__ e, const int32_t *__restrict__ f, OutT *__restrict__ C,
-          int ldc, uint32_t *__restrict__ Xout, const CrtConsts cc) {
+          int ldc, uint32_t *__restrict__ Xout, const CrtConsts cc, int *status) {
   constexpr int LW = Limbs<N>::LW, LX = Limbs<N>::LX;
   const int g = blockIdx.x * kThreads + threadIdx.x;
   if (g >= groups) return;
@@ -59,7 +59,9 @@ __global__ void __launch_bounds__(kThreads)
   if (j0 + 4 <= n) {
 #pragma unroll
     for (int l = 0; l < N; l++)
-      r4[l] = __ldg(reinterpret_cast<const uint32_t *>(src + l * plane)) ^ 0x80808080u;
+      r4[l] = OS2_DBG_GUARD(i < m && j0 + 4 <= ldcres, status)
+                  ? __ldg(reinterpret_cast<const uint32_t *>(src + l * plane)) ^ 0x80808080u
+                  : 0x80808080u;
   } else {
 #pragma unroll
     for (int l = 0; l < N; l++) {
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     const bool neg = (int32_t)x[LX - 1] < 0;
-    if (Xout) {
+    if (Xout && OS2_DBG_GUARD(i < m && j < n, status)) {
       uint32_t *xo = Xout + ((size_t)i * n + j) * 8;
 #pragma unroll
       for (int v = 0; v < 8; v++) xo[v] = v < LX ? x[v < LX ? v : 0] : (neg ? 0xFFFFFFFFu : 0u);
@@ -153,19 +155,27 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int v = 0; v < LX; v++) mag[v] = x[v];
     }
-    C[(size_t)i * ldc + j] = round_scaled_fast<OutT, LX>(mag, neg, ei + f[j]);
+    // |X| <= P/2 < 2^(32 LW): the top limb of the window is zero, and the
+    // normal-range fast path reads the LW limbs below it
+    uint32_t magw[LW];
+#pragma unroll
+    for (int v = 0; v < LW; v++) magw[v] = mag[v];
+    if (OS2_DBG_GUARD(i < m && j < n && n <= ldc, status))
+      C[(size_t)i * ldc + j] = round_scaled_top<OutT, LW>(magw, neg, ei + f[j]);
   }
   }
 }
 
 template <typename OutT>
 cudaError_t crt_t(int m, int n, const int8_t *c, int ldcres, const int32_t *e, const int32_t *f,
-                  OutT *C, int ldc, uint32_t *X_out, const Os2Tables *t, cudaStream_t s) {
+                  OutT *C, int ldc, uint32_t *X_out, const Os2Tables *t, cudaStream_t s,
+                  int *status) {
   const int groups = (n + 3) / 4;
   const dim3 grid((groups + kThreads - 1) / kThreads, m < 65535 ? m : 65535);
 #define OS2_CASE(NN)                                                                              \
   case NN:                                                                                        \
-    k_crt<NN, OutT><<<grid, kThreads, 0, s>>>(m, n, groups, c, ldcres, e, f, C, ldc, X_out, t->crt); \
+    k_crt<NN, OutT><<<grid, kThreads, 0, s>>>(m, n, groups, c, ldcres, e, f, C, ldc, X_out, t->crt, \
+                                              status);                                        \
     break;
   switch (t->N) {
     OS2_CASE(1) OS2_CASE(2) OS2_CASE(3) OS2_CASE(4) OS2_CASE(5) OS2_CASE(6) OS2_CASE(7)
@@ -181,8 +191,10 @@ cudaError_t crt_t(int m, int n, const int8_t *c, int ldcres, const int32_t *e, c
 
 cudaError_t launch_crt(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
                        const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
-                       cudaStream_t s) {
+                       cudaStream_t s, int *status) {
   if (m <= 0 || n <= 0) return cudaSuccess;
-  return f32 ? crt_t<float>(m, n, c, ldcres, e, f, static_cast<float *>(C), ldc, X_out, t, s)
-             : crt_t<double>(m, n, c, ldcres, e, f, static_cast<double *>(C), ldc, X_out, t, s);
+  return f32 ? crt_t<float>(m, n, c, ldcres, e, f, static_cast<float *>(C), ldc, X_out, t, s,
+                            status)
+             : crt_t<double>(m, n, c, ldcres, e, f, static_cast<double *>(C), ldc, X_out, t, s,
+                             status);
 }

@@ -247,8 +247,9 @@ __global__ void __launch_bounds__(kThreads, 512 / (2 * kU * Shape<N>::NMMA))
 #pragma unroll
     for (int q = 0; q < MPW; q++) {
       const int l = warp + kWarps * q;
-      raw[q] = (l < N && j < ldcres) ? ldg16(src + (size_t)(l < N ? l : 0) * plane)
-                                     : make_uint4(0, 0, 0, 0);
+      raw[q] = (l < N && j < ldcres && OS2_DBG_GUARD(i < m && j + 16 <= ldcres, status))
+                   ? ldg16(src + (size_t)(l < N ? l : 0) * plane)
+                   : make_uint4(0, 0, 0, 0);
     }
   };
   // exponent sums e_i + f_j of this thread's two entries of a round
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 512 / (2 * kU * Shape<N>::NMMA))
 #pragma unroll
     for (int h = 0; h < 2; h++) {
       const int j = jr + (2 * half + h) * 128 + quarter * 32 + lane;
-      if (j < n)
+      if (j < n && OS2_DBG_GUARD(i < m && n <= ldc, status))
         finish_entry<N, OutT>(v[h], cc, ef[h], C + (size_t)i * ldc + j,
                               Xout ? Xout + ((size_t)i * n + j) * 8 : nullptr);
     }

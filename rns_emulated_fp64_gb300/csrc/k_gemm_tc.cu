@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               r = r < lo ? r + p : r;
               packed[i >> 2] |= ((uint32_t)(int)r & 0xFFu) << (8 * (i & 3));
             }
-            if (grow < sp.m) {
+            if (grow < sp.m && OS2_DBG_GUARD(l < gc.N && sp.n <= ldo, status)) {
               const int cb = col0 + g * 32;
               if (cb + 32 <= sp.n) {
                 uint4 *d4 = reinterpret_cast<uint4 *>(dst + g * 32);
@@ -463,8 +463,9 @@ struct BoundSeg {
 // The partial sums move as 16-byte vectors (ldp is a multiple of 4), and a
 // group's partial loads are issued before its TMEM load is waited on.
 __device__ __forceinline__ void bound_epilogue(uint32_t taddr, int grow, int col0, int lane,
-                                               const Sched &sp, const BoundSeg &bs) {
-  const bool row_ok = grow < sp.m;
+                                               const Sched &sp, const BoundSeg &bs, int *status) {
+  const bool row_ok =
+      grow < sp.m && OS2_DBG_GUARD((bs.first && bs.last) || sp.n <= bs.ldp, status);
   int rmax = 0;
 #pragma unroll 1
   for (int g = 0; g < 256 / 32; g++) {
@@ -832,7 +833,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(I8 ? kThreads + kCon
       const uint32_t taddr = lane_base + (uint32_t)(buf * BN);
       if (BOUND) {
         bound_epilogue(taddr, tm * 2 * kHalf + (int)rank * kHalf + r_in_tile, tn * BN, lane, sp,
-                       bs);
+                       bs, status);
       } else if (c != sp.nchunks - 1) {
         // intermediate chunk: reduce in place (|r| <= p/2 + 1 carries into the next chunk)
 #pragma unroll 1
@@ -863,7 +864,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(I8 ? kThreads + kCon
                               residue_byte(__uint_as_float(v[4 * i + 1]), p, invp),
                               residue_byte(__uint_as_float(v[4 * i + 2]), p, invp),
                               residue_byte(__uint_as_float(v[4 * i + 3]), p, invp));
-          if (grow < sp.m) {
+          if (grow < sp.m && OS2_DBG_GUARD(l < gc.N && sp.n <= ldo, status)) {
             const int cb = col0 + g * 32;
             if (cb + 32 <= sp.n) {
               uint4 *d4 = reinterpret_cast<uint4 *>(dst + g * 32);

@@ -204,6 +204,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
     for (int ch = blockIdx.x * kThreads + threadIdx.x; ch < cpr; ch += gridDim.x * kThreads) {
       const int h0 = ch * EPT;
+      if (!OS2_DBG_GUARD(row < rs.rows && rs.prow >= rs.rows && h0 + EPT <= kp && k <= kp &&
+                             k <= rs.ldx,
+                         status))
+        continue;
       T v[EPT];
       if (vec && h0 + EPT <= k) {
 #pragma unroll

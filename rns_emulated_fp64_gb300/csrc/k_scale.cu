@@ -218,6 +218,8 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
   const int row = isA ? (int)blockIdx.x : (int)blockIdx.x - a.rows;
   const T *x = reinterpret_cast<const T *>(rs.X) + (size_t)row * rs.ldx;
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & (2 * sizeof(T) - 1)) == 0);
+  if (!OS2_DBG_GUARD(row < rs.rows && k <= rs.ldx && (MODE != SM_BARS || k <= kp), status))
+    return;  // (uniform over the CTA)
 
   // pass 1: the largest key of the row.  For doubles only the high words are
   // loaded, sixteen 4-byte loads per thread in flight: the same DRAM sectors
@@ -287,7 +289,8 @@ __global__ void __launch_bounds__(NT, 2048 / NT)
           v[u] = __float2half_rn((float)ceil_shift(d.mant, d.ex2 + 6 - E));
         }
       }
-      *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
+      if (OS2_DBG_GUARD(h0 + 8 <= kp, status))
+        *reinterpret_cast<uint4 *>(dst + h0) = *reinterpret_cast<uint4 *>(v);
     }
     return;
   }

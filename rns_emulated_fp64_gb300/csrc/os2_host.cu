@@ -390,7 +390,7 @@ cudaError_t crt_launch(bool f32, int m, int n, const int8_t *c, int ldcres, cons
                        int *status, cudaStream_t s, bool beside = false) {
   if (crt_on_tc(ldcres, c, beside))
     return launch_crt_tc(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, status, s);
-  return launch_crt(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, s);
+  return launch_crt(f32, m, n, c, ldcres, e, f, C, ldc, X_out, t, s, status);
 }
 
 template <typename T>
@@ -636,8 +636,9 @@ os2_status run_gemm_panels(bool f32, int m, int n, int k, const void *A, int lda
     OS2_TRY(cudaEventRecord(p->g_done[i], s));
     OS2_TRY(cudaStreamWaitEvent(p->crt, p->g_done[i], 0));
     ProfScope ps("crt_unscale", p->crt);
+    // the last panel's reconstruction has no product left beside it
     OS2_TRY(crt_launch(f32, mi, n, ci, L.ldcres, e + r0, f, Cb + (size_t)r0 * ldc * es, ldc,
-                       nullptr, t, status, p->crt, true));
+                       nullptr, t, status, p->crt, i + 1 < P));
   }
   // `stream` covers everything: it waits for the last reconstruction
   OS2_TRY(cudaEventRecord(p->done, p->crt));
@@ -950,7 +951,7 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
   // steps 3-5 for the block (row panel i, columns c0 .. c0+nj of column
   // panel j, or all columns when j < 0), then its copy out
   int blocks = 0;
-  auto block = [&](int i, int j, int c0, int nj) -> os2_status {
+  auto block = [&](int i, int j, int c0, int nj, bool last) -> os2_status {
     const int r0 = i * mp, mi = std::min(mp, m - r0);
     if (side) {
       // the split stream runs in arrival order: A_0, B_0 .. B_{Q-1}, A_1 ..
@@ -973,9 +974,10 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
     }
     // the block's CRT: the CUDA-core kernel runs on the CRT stream beside the
     // next block's product; the tensor-core one follows the product on `stream`
+    // (the last block has no product left beside it)
     cudaEvent_t gd = p->g_done[blocks], done = p->c_done[blocks];
     blocks++;
-    const bool tc = crt_on_tc(L.ldcres, ci, true);
+    const bool tc = crt_on_tc(L.ldcres, ci, !last);
     cudaStream_t cs = tc ? s : p->crt;
     if (!tc) {
       if ((err = cudaEventRecord(gd, s))) return cuda_status(err);
@@ -993,10 +995,10 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
                                  mi, cudaMemcpyDeviceToHost, p->out));
   };
   auto row_panel = [&](int i, bool by_blocks) -> os2_status {
-    if (!by_blocks) return block(i, -1, 0, n);
+    if (!by_blocks) return block(i, -1, 0, n, i == P - 1);
     for (int j = 0; j < Q; j++) {
       const int c0 = j * nq;
-      if ((st = block(i, j, c0, std::min(nq, n - c0)))) return st;
+      if ((st = block(i, j, c0, std::min(nq, n - c0), i == P - 1 && j == Q - 1))) return st;
     }
     return OS2_OK;
   };
@@ -1246,6 +1248,7 @@ const char *os2_status_string(int status) {
     case OS2_ERR_RANGE: return "scaled integer out of range (|trunc(x 2^e)| >= 2^89)";
     case OS2_ERR_TIMEOUT: return "device-side wait timed out";
     case OS2_ERR_CUDA: return "CUDA error";
+    case OS2_ERR_BOUNDS: return "index check failed (debug build)";
   }
   return "unknown status";
 }

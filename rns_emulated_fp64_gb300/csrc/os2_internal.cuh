@@ -7,6 +7,17 @@
 
 #include "os2.h"
 
+// Debug build (compiled with -DOS2_DEBUG): the kernels check the index of each
+// hand-computed global access against the extent of the array it addresses;
+// a failed check records OS2_ERR_BOUNDS in the status word and skips the
+// access.  In the release build the checks compile to nothing.
+#ifdef OS2_DEBUG
+#define OS2_DBG_GUARD(cond, status) \
+  ((cond) ? true : (((status) ? atomicCAS((status), 0, (int)OS2_ERR_BOUNDS) : 0), false))
+#else
+#define OS2_DBG_GUARD(cond, status) true
+#endif
+
 #define OS2_MAX_MODULI 20
 #define OS2_KP_ALIGN 64          // residue-plane row pitch granularity (one 128-byte k-block)
 #define OS2_CRES_ALIGN 16        // int8 product-residue row pitch granularity
@@ -113,7 +124,7 @@ cudaError_t launch_accu_exponents(const int32_t *bound, const int32_t *E, int ro
 // f32: C is float (correctly rounded to binary32) instead of double.
 cudaError_t launch_crt(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
                        const int32_t *f, void *C, int ldc, uint32_t *X_out, const Os2Tables *t,
-                       cudaStream_t s);
+                       cudaStream_t s, int *status = nullptr);
 // Steps 4 + 5 on the tensor cores; needs ldcres % 16 == 0 and a 16-byte
 // aligned c (else cudaErrorInvalidValue).
 cudaError_t launch_crt_tc(bool f32, int m, int n, const int8_t *c, int ldcres, const int32_t *e,
