@@ -90,9 +90,6 @@ struct Shape {
   static_assert(SMEM_USED <= SMEM, "shared memory layout exceeds its padding");
 };
 
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ uint4 ldg16(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -386,13 +383,6 @@ __global__ void __launch_bounds__(kThreads, 512 / (2 * kU * Shape<N>::NMMA))
   }
 }
 
-int sm_count() {
-  int dev = 0, v = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-  return v > 0 ? v : 1;
-}
-
 template <int N, typename OutT>
 cudaError_t launch_n(int m, int n, const int8_t *c, int ldcres, const int32_t *e, const int32_t *f,
                      OutT *C, int ldc, uint32_t *X_out, const Os2Tables *t, int *status,
@@ -406,7 +396,7 @@ cudaError_t launch_n(int m, int n, const int8_t *c, int ldcres, const int32_t *e
   const int segs = (n + kSeg - 1) / kSeg;
   const long long rounds = (long long)m * segs;
   if (rounds > (1LL << 31) - 1) return cudaErrorInvalidValue;
-  const int grid = (int)std::min<long long>(rounds, (long long)sm_count() * S::PER_SM);
+  const int grid = (int)std::min<long long>(rounds, (long long)os2_sm_count() * S::PER_SM);
   k_crt_tc<N, OutT><<<grid, kThreads, S::SMEM, s>>>(m, n, segs, (int)rounds, c, ldcres, e, f, C,
                                                    ldc, X_out, t->crt_tc, status);
   return cudaGetLastError();

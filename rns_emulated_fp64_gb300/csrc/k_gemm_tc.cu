@@ -402,20 +402,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 2-SM variant of KIND 0: a CTA pair (cluster of 2) computes a 256x256 tile
 // with tcgen05.mma.cta_group::2 issued by the even CTA.  Each CTA loads 128
 // rows of the A tile and 128 rows of the B tile (its half of N) into a ring
-// of 3 stages of two k-blocks; both CTAs' copies complete on the even CTA's
-// "full" barrier,
+// of kStages2 stages of kKbStage2 k-blocks; both CTAs' copies complete on the
+// even CTA's "full" barrier,
 // the MMA commits are multicast to both CTAs' "empty" and "accumulator full"
 // barriers, and both CTAs' epilogues release an accumulator on the even
 // CTA's "accumulator empty" barrier.  Each CTA's TMEM holds its 128 rows x
 // 256 columns of the two interleaved jobs, reduced mod p like the single-SM
 // kernel's (with FMA-only rounding, see above).  Chunks are counted in stages:
-// at most 7 stages (896 terms) between reductions.  Per SM this halves the
-// B-tile traffic of the single-SM kernel.
+// at most 7 stages of two k-blocks (896 terms) between reductions.  Per SM
+// this halves the B-tile traffic of the single-SM kernel.
 // A stage holds two k-blocks (128 terms): one operand wait, fence and commit
-// per eight MMAs instead of per four.
+// per eight MMAs.  Measured at 8192^3 with 16 moduli, the same shared memory
+// cut into 6 or 7 stages of one k-block ran 4.5 % slower.
+constexpr int kKbStage2 = 2;  // k-blocks per stage
 constexpr int kStages2 = 3;
 constexpr int kHalf = 128;
-constexpr int BK2 = 2 * BK;  // terms per stage of the 2-SM kernel
+constexpr int BK2 = 2 * BK;  // terms per stage of the int8-plane variant
 
 // ---------------------------------------------- 2-SM epilogue arithmetic
 // Accumulators hold exact integers |x| < 2^24.  Adding 1.5 * 2^23 rounds a
@@ -445,12 +447,12 @@ __device__ __forceinline__ uint32_t pack4(uint32_t a, uint32_t b, uint32_t c, ui
 }
 
 // Accurate-mode bound product on the 2-SM kernel (BOUND = 1): one launch per
-// segment of at most 32 stages (4096 terms), whose FP32 sums (Abar, Bbar <= 64, so each
+// segment of at most 4096 terms, whose FP32 sums (Abar, Bbar <= 64, so each
 // product <= 2^12 and a segment's sum <= 2^24) are exact.  Segments after the
 // first add the int32 partial sums of the earlier ones; the last takes the
 // row and column maxima.
 struct BoundSeg {
-  int kb_begin;          // first stage (pair of k-blocks) of the segment
+  int kb_begin;          // first stage of the segment
   int first, last;       // segment flags
   int32_t *partial;      // int32 [m][ldp] partial sums between segments
   int ldp;
@@ -537,9 +539,15 @@ constexpr int kStages2I8 = 2;      // FP16 operand stages of the int8 variant
 constexpr int kRawStages2 = 3;     // int8 stages
 constexpr int kConvThreads = 256;  // converter warps 6-13
 
+// k-blocks per FP16 operand stage: the int8-plane variant converts two at a time
+template <int I8>
+constexpr int kb_per_stage2() {
+  return I8 ? 2 : kKbStage2;
+}
+
 template <int I8>
 constexpr size_t smem2_bytes() {
-  return 1024 + (size_t)(I8 ? kStages2I8 : kStages2) * 2 * 2 * kHalf * BK * 2 +
+  return 1024 + (size_t)(I8 ? kStages2I8 : kStages2) * kb_per_stage2<I8>() * 2 * kHalf * BK * 2 +
          (I8 ? (size_t)kRawStages2 * 2 * kHalf * BK2 : 0) + 256;
 }
 
@@ -561,9 +569,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(I8 ? kThreads + kCon
                const Sched sp, const GemmConsts gc, int8_t *__restrict__ out, int ldo,
                const BoundSeg bs, int *status) {
   constexpr int BN = 256, STAGES = I8 ? kStages2I8 : kStages2;
+  constexpr int KPS = kb_per_stage2<I8>();  // k-blocks per FP16 stage
   constexpr int RSTAGES = I8 ? kRawStages2 : 0;
   constexpr uint32_t HALF = kHalf * BK * 2;  // one k-block of 128 rows
-  constexpr uint32_t A_BYTES = 2 * HALF, B_BYTES = 2 * HALF;
+  constexpr uint32_t A_BYTES = KPS * HALF, B_BYTES = KPS * HALF;
   constexpr uint32_t RAW_HALF = kHalf * BK2;  // int8 stage: 128 rows x 128 bytes of A (or B)
   constexpr uint32_t RAW_BYTES = 2 * RAW_HALF;
   constexpr uint32_t IDESC = idesc_f16_f32(2 * kHalf, BN);
@@ -739,9 +748,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(I8 ? kThreads + kCon
           const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A_BYTES + B_BYTES));
           // a stage past the last k-block reads zeros (out-of-range box)
-          const int kx = (BOUND ? bs.kb_begin + kb : kb) * BK2;
+          const int kx = (BOUND ? bs.kb_begin + kb : kb) * (KPS * BK);
 #pragma unroll
-          for (int h = 0; h < 2; h++) {
+          for (int h = 0; h < KPS; h++) {
             tma_load_3d_pair(sA + stage * A_BYTES + h * HALF, &mapA, fbar, kx + h * BK,
                              tm * 2 * kHalf + (int)rank * kHalf, l);
             tma_load_3d_pair(sB + stage * B_BYTES + h * HALF, &mapB, fbar, kx + h * BK,
@@ -787,7 +796,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(I8 ? kThreads + kCon
           }
           tc_fence_after();
 #pragma unroll
-          for (int h = 0; h < 2; h++) {
+          for (int h = 0; h < KPS; h++) {
             const uint64_t ad = sdesc_k128(smem_u32(sA + stage * A_BYTES + h * HALF));
             const uint64_t bd = sdesc_k128(smem_u32(sB + stage * B_BYTES + h * HALF));
 #pragma unroll
@@ -924,13 +933,6 @@ bool make_map(CUtensorMap *map, const void *base, int kp, int rows, int nplanes,
   return r == CUDA_SUCCESS;
 }
 
-int num_sms() {
-  int dev = 0, v = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-  return v > 0 ? v : 1;
-}
-
 template <int KIND>
 cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int nplanes, void *out,
                    int ldo, int32_t *rowmax, int32_t *colmax, int prod_bound_log2,
@@ -964,7 +966,7 @@ cudaError_t launch(int m, int n, int kp, const void *RA, const void *RB, int npl
   if (sp.chunk < 1) return cudaErrorInvalidValue;
   sp.nchunks = (sp.kb_total + sp.chunk - 1) / sp.chunk;
   if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
-  const int grid = std::min(num_sms(), sp.njobs);
+  const int grid = std::min(os2_sm_count(), sp.njobs);
   GemmConsts gc = t ? t->gemm : GemmConsts{};
   k_gemm_tc<KIND><<<grid, kThreads, smem, s>>>(ma, mb, sp, gc, out, ldo, rowmax, colmax, status);
   return cudaGetLastError();
@@ -1024,12 +1026,13 @@ cudaError_t launch2(int m, int n, int kp, const void *RA, const void *RB, int np
                        : make_map(&ma, RA, kp, m, nplanes, kHalf, m) &&
                              make_map(&mb, RB, kp, n, nplanes, kHalf, b_plane_rows);
   if (!maps) return cudaErrorInvalidValue;
-  // the 2-SM kernel counts k in stages of two k-blocks
-  Sched sp = sched2(m, n, (kp / BK + 1) / 2, nplanes);
-  sp.chunk = (int)(((1LL << 24) - 135) / ((long long)BK2 << 14));
+  // the 2-SM kernel counts k in stages of kps k-blocks
+  const int kps = i8 ? kb_per_stage2<1>() : kb_per_stage2<0>();
+  Sched sp = sched2(m, n, (kp / BK + kps - 1) / kps, nplanes);
+  sp.chunk = (int)(((1LL << 24) - 135) / ((long long)(kps * BK) << 14));
   sp.nchunks = (sp.kb_total + sp.chunk - 1) / sp.chunk;
   if (sp.njobs == 0 || sp.nchunks == 0) return cudaSuccess;
-  const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
+  const int pairs = std::min(std::max(os2_sm_count() / 2, 1), sp.njobs);
   GemmConsts gc = t ? t->gemm : GemmConsts{};
   if (i8)
     k_gemm_tc2<0, 1><<<2 * pairs, kThreads + kConvThreads, smem, s>>>(
@@ -1047,13 +1050,14 @@ cudaError_t launch2_bound(int m, int n, int kp, const void *RA, const void *RB, 
                           int ldp, int32_t *rowmax, int32_t *colmax, int *status,
                           cudaStream_t s) {
   constexpr size_t smem = smem2_bytes<0>();
-  constexpr int kSegMax = (int)((1LL << 24) / ((long long)BK2 << 12));  // 32 stages, 4096 terms
+  constexpr int kps = kb_per_stage2<0>();
+  constexpr int kSegMax = (int)((1LL << 24) / ((long long)(kps * BK) << 12));  // 4096 terms
   cudaError_t attr_err = set_smem2<1>();
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
   if (!make_map(&ma, RA, kp, m, 1, kHalf, m) || !make_map(&mb, RB, kp, n, 1, kHalf, n))
     return cudaErrorInvalidValue;
-  const int kb_all = (kp / BK + 1) / 2;
+  const int kb_all = (kp / BK + kps - 1) / kps;
   const int segs = (kb_all + kSegMax - 1) / kSegMax;
   if (segs > 1 && (!partial || ldp < n || ldp % 4 != 0 ||
                    (reinterpret_cast<uintptr_t>(partial) & 15)))
@@ -1064,7 +1068,7 @@ cudaError_t launch2_bound(int m, int n, int kp, const void *RA, const void *RB, 
     sp.chunk = sp.kb_total;
     sp.nchunks = 1;
     if (sp.njobs == 0 || sp.kb_total == 0) return cudaSuccess;
-    const int pairs = std::min(std::max(num_sms() / 2, 1), sp.njobs);
+    const int pairs = std::min(std::max(os2_sm_count() / 2, 1), sp.njobs);
     const BoundSeg bs{kb0, g == 0, g == segs - 1, partial, ldp, rowmax, colmax};
     k_gemm_tc2<1><<<2 * pairs, kThreads, smem, s>>>(ma, mb, sp, GemmConsts{}, nullptr, 0, bs,
                                                     status);

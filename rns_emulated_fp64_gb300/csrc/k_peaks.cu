@@ -53,10 +53,6 @@ __device__ __forceinline__ void fill_tile(uint8_t *tile, int rows, int row0, boo
   }
 }
 
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Compares this thread's TMEM lane (row `arow` of D, 256 columns) with the
 // exact product of the formula operands.
 __device__ __forceinline__ int check_row(uint32_t lane_addr, int arow) {
@@ -216,13 +212,6 @@ __global__ void __launch_bounds__(256) k_peak_s8(int iters, int check, int32_t *
   }
 }
 
-int sm_count() {
-  int dev = 0, v = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-  return v > 0 ? v : 1;
-}
-
 template <int PAIR>
 cudaError_t launch_f16(int iters, int check, int32_t *result, int *status, cudaStream_t s,
                        double *flop) {
@@ -230,7 +219,7 @@ cudaError_t launch_f16(int iters, int check, int32_t *result, int *status, cudaS
   cudaError_t e = cudaFuncSetAttribute(k_peak_f16<PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e) return e;
-  const int sms = sm_count();
+  const int sms = os2_sm_count();
   const int grid = PAIR ? (sms / 2) * 2 : sms;
   if (flop) *flop = (double)(PAIR ? grid / 2 : grid) * iters * 4.0 * 2.0 * (PAIR ? 256 : 128) * 256 * 16;
   if (PAIR) {
@@ -261,7 +250,7 @@ cudaError_t launch_peak_probe(int kind, int iters, int check, int32_t *result, i
   if (kind == OS2_PROBE_F16_1SM) return launch_f16<0>(iters, check, result, status, s, flop);
   if (kind == OS2_PROBE_F16_2SM) return launch_f16<1>(iters, check, result, status, s, flop);
   if (kind == OS2_PROBE_S8_SYNC) {
-    const int grid = sm_count() * 4;
+    const int grid = os2_sm_count() * 4;
     if (flop) *flop = (double)grid * 8 * iters * 8.0 * 2.0 * 16 * 8 * 32;
     k_peak_s8<<<grid, 256, 0, s>>>(iters, check, result);
     return cudaGetLastError();

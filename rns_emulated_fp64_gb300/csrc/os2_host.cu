@@ -17,6 +17,13 @@
 // ---------------------------------------------------------------------------
 __device__ int g_os2_status;
 
+int os2_sm_count() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  return v > 0 ? v : 1;
+}
+
 int *os2_status_ptr() {
   static std::mutex mu;
   static int *ptrs[64] = {};

@@ -95,6 +95,9 @@ const Os2Tables *os2_tables(int N);
 // Per-device status word (device address), set up on first use.
 int *os2_status_ptr();
 
+// Number of SMs of the current device (at least 1).
+int os2_sm_count();
+
 // One CTA whose bounded mbarrier waits run out (failure-detection self-test).
 cudaError_t launch_wait_selftest(long long limit, int *status, int32_t *result, cudaStream_t s);
 

@@ -56,14 +56,32 @@ SHAPES = [(64, 64, 64), (1, 1, 1), (3, 5, 7), (129, 257, 65), (300, 520, 1000), 
 # ------------------------------------------------------------------ step 1 --
 @pytest.mark.parametrize("kind,phi", [("normal", 0.0), ("spread", 0.5), ("spread", 4.0)])
 @pytest.mark.parametrize("N", [2, 12, 16, 20])
-def test_scale_fast_parity(kind, phi, N):
-    A, Bt = workloads.make_pair(kind, 257, 130, 777, seed=N, phi=phi)
+@pytest.mark.parametrize("k", [777, 778, 9216, 9218])
+def test_scale_fast_parity(kind, phi, N, k):
+    """Rows of 256-thread (k <= 8192) and 512-thread CTAs, odd k (rows that
+    alternate between 16-byte aligned and not, so both the two-entry vector
+    loads and the scalar loads run) and even k.  Zero rows, subnormal-only
+    rows and entries."""
+    A, Bt = workloads.make_pair(kind, 257, 130, k, seed=N, phi=phi)
     A[5] = 0.0
     A[7, ::3] = 5e-324
+    A[9] = 5e-324
     e, f = os2.scale(dev(A), dev(Bt), N, "fast")
     status_ok()
     assert np.array_equal(e.cpu().numpy(), orc.scale_fast(A, N))
     assert np.array_equal(f.cpu().numpy(), orc.scale_fast(Bt, N))
+
+
+def test_scale_fast_nonfinite_sets_status():
+    """Inf in a row of A, then NaN in a column of B, set the status word."""
+    A, Bt = workloads.make_pair("normal", 40, 30, 1024, seed=1)
+    A[3, 17] = np.inf
+    os2.scale(dev(A), dev(Bt), 16, "fast")
+    assert os2.get_status() == os2.binding.ERR_NONFINITE
+    Bt[2, 5] = np.nan
+    A[3, 17] = 1.0
+    os2.scale(dev(A), dev(Bt), 16, "fast")
+    assert os2.get_status() == os2.binding.ERR_NONFINITE
 
 
 @pytest.mark.parametrize("N", [4, 14, 20])
