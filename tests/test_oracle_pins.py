@@ -262,6 +262,38 @@ def test_accurate_scaling_bound_and_bigref():
                     assert R[i] * Fraction(4) ** g <= H < R[i] * Fraction(4) ** (g + 1)
 
 
+def test_accurate_scaling_worked_example():
+    """The accurate-mode reading of [Q] 手順1と5 / [G] Problemstellung 1 (one
+    extra INT8 product bounds |A||B|), worked by hand on a 2 x 3 by 3 x 2
+    product with 4 moduli, so that a slip in the magnitude planes' width or
+    rounding, in the bound product or in the exponent search fails here
+    whatever the other restatements do.
+
+    Tight exponents (|x| < 2^E): rows of A 1, 2; columns of B 1, 0.
+    Magnitude planes ceil(|x| 2^(6 - E)):
+      row 0 * 32: 1, 0.5, 0.3 -> 32, 16, 10 (9.6 rounds up)
+      row 1 * 16: 3, 2.5, 0   -> 48, 40, 0
+      col 0 * 32: 0.25, 0.25, 1 -> 8, 8, 32
+      col 1 * 64: 0.1, 0.7, 0   -> 7, 45, 0 (6.4 and 44.8 round up)
+    Bound product: [[32*8 + 16*8 + 10*32, 32*7 + 16*45], [48*8 + 40*8, 48*7 + 40*45]]
+                 = [[704, 944], [704, 2136]]
+    R = row maxima (944, 2136), K = column maxima (704, 2136).
+    N = 4: P = 256*255*253*251 = 4145475840, H = 2072737919.
+    Largest g with R 4^g <= H: 944 -> 10 (944*4^10 = 989855744), 2136 -> 9
+    (2136*4^9 = 559939584, 2136*4^10 > H), 704 -> 10 (704*4^10 = 738197504).
+    e = g + 6 - E: row 0 10 + 5 = 15, row 1 9 + 4 = 13; f: col 0 10 + 5 = 15,
+    col 1 9 + 6 = 15."""
+    A = np.array([[1.0, 0.5, 0.3], [-3.0, 2.5, 0.0]])
+    Bt = np.array([[0.25, 0.25, 1.0], [0.1, -0.7, 0.0]])
+    P, H, _, _ = orc.tables(4)
+    assert (P, H) == (4145475840, 2072737919)
+    e, f, R, K = orc.scale_accu(A, Bt, 4, return_bounds=True)
+    assert list(R) == [944, 2136]
+    assert list(K) == [704, 2136]
+    assert list(e) == [15, 13]
+    assert list(f) == [15, 15]
+
+
 # ------------------------------------------------------- full pipeline ------
 def _rand_special(rng, m, k):
     A = rng.standard_normal((m, k)) * np.exp2(rng.integers(-30, 30, size=(m, k)))
