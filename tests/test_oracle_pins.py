@@ -294,6 +294,33 @@ def test_accurate_scaling_worked_example():
     assert list(f) == [15, 15]
 
 
+def test_fast_scaling_worked_example():
+    """The fast (revised) scaling of [G] Methodik 1, with its log2 of the sum
+    of squares replaced by the exact upper bound Q = sum ceil(|x| 2^(23-E))^2,
+    worked by hand on the operands of the accurate-mode example, 4 moduli
+    (H = 2072737919).  E as there: rows 1, 2; columns 1, 0.
+      row 0 * 2^22: 1, 0.5, 0.3 -> 4194304, 2097152, 1258292 (1258291.2 up)
+        Q = 2^44 + 2^42 + 1258292^2 = 23573531312784
+      row 1 * 2^21: 3, 2.5, 0 -> 6291456, 5242880, 0
+        Q = 6291456^2 + 5242880^2 = 67070209294336
+      col 0 * 2^22: 0.25, 0.25, 1 -> 1048576, 1048576, 4194304
+        Q = 2 * 2^40 + 2^44 = 19791209299968
+      col 1 * 2^23: 0.1, 0.7, 0 -> 838861, 5872026, 0 (838860.8, 5872025.6 up)
+        Q = 838861^2 + 5872026^2 = 35184377121997
+    Largest g with Q 4^g <= H: -7 (Q / 4^7 = 1438814167.04; / 4^6 > H),
+    -8 (Q / 4^8 = 1023410176; / 4^7 > H), -7 (1207959552; / 4^6 > H),
+    -8 (536870988.8; / 4^7 = 2147483955.2 > H).  e = g + 23 - E: 15, 13;
+    f: 15, 15."""
+    A = np.array([[1.0, 0.5, 0.3], [-3.0, 2.5, 0.0]])
+    Bt = np.array([[0.25, 0.25, 1.0], [0.1, -0.7, 0.0]])
+    e, Qa = orc.scale_fast(A, 4, return_Q=True)
+    f, Qb = orc.scale_fast(Bt, 4, return_Q=True)
+    assert [int(x) for x in Qa] == [23573531312784, 67070209294336]
+    assert [int(x) for x in Qb] == [19791209299968, 35184377121997]
+    assert list(e) == [15, 13]
+    assert list(f) == [15, 15]
+
+
 # ------------------------------------------------------- full pipeline ------
 def _rand_special(rng, m, k):
     A = rng.standard_normal((m, k)) * np.exp2(rng.integers(-30, 30, size=(m, k)))
