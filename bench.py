@@ -63,9 +63,10 @@ def parse():
                     help="skip the tensor-pipe peak probes (own kernels) before the timed steps")
     ap.add_argument("--crt", default="default", choices=["default", "tc", "simt", "auto"],
                     help="kernel of steps 4 + 5 (os2_set_crt_variant); default: the library's")
-    ap.add_argument("--gemm", default="tc", choices=["tc", "tc_1sm", "tc_i8", "simt"],
+    ap.add_argument("--gemm", default="tc", choices=["tc", "tc_1sm", "tc_i8", "s8", "simt"],
                     help="step-3 kernel (os2_set_gemm_variant): tc (default), tc_1sm, tc_i8 "
-                         "(int8 residue planes widened on chip) or simt")
+                         "(int8 residue planes widened on chip), s8 (mma.sync s8 on int8 "
+                         "planes; its roofline is the own mma.sync s8 probe) or simt")
     ap.add_argument("--accuracy", action="store_true",
                     help="error against the exact product for 1024^3, phi in {0.5,2,4}, N in "
                          "{12..20}, both modes, beside native DGEMM; prints one JSON line")
@@ -334,7 +335,7 @@ def run_ours(a):
     world, rank, local = dist_setup(a)
     dev = torch.device("cuda", local if world > 1 else 0)
     os2.set_gemm_variant({"tc": os2.GEMM_TC, "tc_1sm": os2.GEMM_TC_1SM, "tc_i8": os2.GEMM_TC_I8,
-                          "simt": os2.GEMM_SIMT}[a.gemm])
+                          "s8": os2.GEMM_S8_SYNC, "simt": os2.GEMM_SIMT}[a.gemm])
     if a.crt != "default":
         os2.set_crt_variant({"tc": os2.CRT_TC, "simt": os2.CRT_SIMT, "auto": os2.CRT_AUTO}[a.crt])
     m, n, k, N = a.m, a.n, a.k, a.num_moduli
@@ -417,7 +418,20 @@ def run_ours(a):
     sustained = timed_s >= 3.0 and "bf16_tflops_sustained" in peaks
     peak_t = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     roofline = None
-    if g:
+    work_launch = "N*2mnk / launches per step = %.4g flop" % (
+        2.0 * N * m * n * k / max(g["launches_per_step"], 1.0)) if g else None
+    if g and a.gemm == "s8" and peaks_probe:
+        # the INT8 tensor path outside tcgen05: its own measured peak (MEASURED_PEAKS.json
+        # holds no INT8 figure), multiply-adds counted as two operations as in the probe
+        s8 = peaks_probe["mma_sync_s8"]["best"]
+        roofline = {"bound": "tensor",
+                    "kernel": "gemm_modp (mma.sync.m16n8k32 s8 x s8 -> s32, int8 residue planes)",
+                    "achieved": g["achieved"], "peak": s8, "unit": "TFLOP/s",
+                    "frac": g["achieved"] / s8, "traffic": None,
+                    "peak_source": "own mma.sync s8 probe of this run (of measured; int8 "
+                                   "operations, multiply-add = 2)",
+                    "work_per_launch": work_launch}
+    elif g:
         roofline = {"bound": "tensor", "kernel": "gemm_modp (tcgen05.mma kind::f16, FP16-held residues)",
                     "achieved": g["achieved"], "peak": peak_t, "unit": "TFLOP/s",
                     "frac": g["achieved"] / peak_t,
@@ -426,8 +440,7 @@ def run_ours(a):
                     "peak_source": "%s bf16 dense %s (of %s; FP16 rate = BF16 rate); timed region "
                                    "%.2f s" % (src, "sustained" if sustained else "burst", src,
                                                timed_s),
-                    "work_per_launch": "N*2mnk / launches per step = %.4g flop"
-                                       % (2.0 * N * m * n * k / max(g["launches_per_step"], 1.0))}
+                    "work_per_launch": work_launch}
         if peaks_probe:
             own = peaks_probe["tcgen05_f16_2sm"]["best"]
             roofline["own_pipe_peak"] = {

@@ -76,10 +76,15 @@ typedef enum {
   OS2_GEMM_TC = 0,        /* tcgen05 2-SM tensor-core kernel, 256x256 tiles (default) */
   OS2_GEMM_SIMT = 1,      /* plain CUDA-core int32 kernel (exact reference, slow) */
   OS2_GEMM_TC_1SM = 2,    /* tcgen05 single-SM tensor-core kernel, 128x256 tiles */
-  OS2_GEMM_TC_I8 = 3      /* as OS2_GEMM_TC, from int8 residue planes in HBM (half the
+  OS2_GEMM_TC_I8 = 3,     /* as OS2_GEMM_TC, from int8 residue planes in HBM (half the
                              bytes of FP16) widened to FP16 on chip by four extra warps;
                              step 2 then writes int8 planes (os2_gemm, os2_gemm_host,
                              os2_sgemm, complex products; not os2_gemm_residues) */
+  OS2_GEMM_S8_SYNC = 4    /* the INT8 tensor path outside tcgen05: mma.sync.m16n8k32
+                             s8 x s8 -> s32 from int8 residue planes, exact int32 sums
+                             (reduced mod p every 65536 terms for mod-p output); step 2
+                             then writes int8 planes, and os2_gemm_residues takes int8
+                             planes for it.  About 12 times slower than OS2_GEMM_TC */
 } os2_gemm_variant;
 
 typedef enum {
@@ -231,7 +236,9 @@ os2_status os2_residues(int rows, int k, const double *X, int ldx, const int32_t
  * split into blocks): N residue matrix products from FP16 planes RA (N x m x ldp)
  * and RB (N x n x ldp), ldp % 64 == 0, k <= ldp.  out_kind selects int8
  * c_l = sym(G_l mod p_l) or raw int32 G_l; out is [N][m][ldo] with ldo >= n
- * (ldo % 16 == 0 for int8, % 4 for int32).  variant: an os2_gemm_variant.
+ * (ldo % 16 == 0 for int8, % 4 for int32).  variant: an os2_gemm_variant
+ * other than OS2_GEMM_TC_I8; with OS2_GEMM_S8_SYNC, RA and RB are int8 planes
+ * (N x m x ldp and N x n x ldp bytes, residues in [-128, 127]) instead of FP16.
  * Raw int32 output with the TC variant runs the exact-accumulation kernel. */
 os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB, int ldp,
                              int num_moduli, int out_kind, void *out, int ldo, int variant,

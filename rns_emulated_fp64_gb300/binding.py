@@ -17,7 +17,7 @@ from . import build as _build
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE = 0, 1, 2, 3
 ERR_NONFINITE, ERR_RANGE, ERR_TIMEOUT, ERR_CUDA, ERR_BOUNDS = 4, 5, 6, 7, 8
 MODE_FAST, MODE_ACCURATE = 0, 1
-GEMM_TC, GEMM_SIMT, GEMM_TC_1SM, GEMM_TC_I8 = 0, 1, 2, 3
+GEMM_TC, GEMM_SIMT, GEMM_TC_1SM, GEMM_TC_I8, GEMM_S8_SYNC = 0, 1, 2, 3, 4
 CRT_TC, CRT_SIMT, CRT_AUTO = 0, 1, 2
 OUT_MODP_INT8, OUT_RAW_INT32 = 0, 1
 KP_ALIGN, CRES_ALIGN = 64, 16
@@ -357,7 +357,8 @@ def residues(X, exps, num_moduli, ldp=None, stream=None) -> torch.Tensor:
 
 
 def gemm_residues(RA, RB, k, out_kind=OUT_MODP_INT8, variant=GEMM_TC, stream=None):
-    """Step 3: N residue products of FP16 planes RA [N,m,ldp], RB [N,n,ldp].
+    """Step 3: N residue products of FP16 planes RA [N,m,ldp], RB [N,n,ldp]
+    (int8 planes for GEMM_S8_SYNC).
     Returns int8 [N, m, ldo] (mod p, symmetric) or int32 [N, m, ldo] (raw)."""
     N, m, ldp = RA.shape
     n = RB.shape[1]

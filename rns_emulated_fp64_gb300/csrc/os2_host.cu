@@ -292,8 +292,11 @@ void build_tables(int N, Os2Tables *t) {
 std::atomic<int> g_variant{OS2_GEMM_TC};
 std::atomic<int> g_crt_variant{OS2_CRT_AUTO};
 
-// The int8-plane step-3 kernel reads int8 residue planes (step 2 writes them so).
-bool planes_i8() { return g_variant.load() == OS2_GEMM_TC_I8; }
+// The int8-plane step-3 kernels read int8 residue planes (step 2 writes them so).
+bool planes_i8() {
+  const int v = g_variant.load();
+  return v == OS2_GEMM_TC_I8 || v == OS2_GEMM_S8_SYNC;
+}
 
 // Optional per-kernel timing: CUDA events recorded on the launching stream
 // around every kernel that os2_gemm enqueues (no synchronisation added).
@@ -432,7 +435,8 @@ bool bound_on_2sm(int m, const Layout &L) {
   const int segs = (L.kp + 4095) / 4096;
   const bool room = L.total - L.cres >= 4 * (size_t)m * (size_t)L.ldcres;
   const int v = g_variant.load();
-  return (v == OS2_GEMM_TC || v == OS2_GEMM_TC_I8) && (segs == 1 || room);
+  return (v == OS2_GEMM_TC || v == OS2_GEMM_TC_I8 || v == OS2_GEMM_S8_SYNC) &&
+         (segs == 1 || room);
 }
 
 // Kernel launches of bound_product.
@@ -484,6 +488,8 @@ os2_status residue_products(int m, int n, const Layout &L, const void *pa, const
   cudaError_t err;
   if (variant == OS2_GEMM_SIMT)
     err = launch_gemm_simt(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, s);
+  else if (variant == OS2_GEMM_S8_SYNC)
+    err = launch_gemm_s8(m, n, L.kp, pa, pb, N, OS2_OUT_MODP_INT8, cres, L.ldcres, t, status, s);
   else
     err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : (variant == OS2_GEMM_TC_I8 ? 3 : 2), m, n, L.kp, pa, pb, N, cres,
                          L.ldcres, nullptr, nullptr, 14, t, status, s);
@@ -974,6 +980,9 @@ os2_status os2_gemm_host(int m, int n, int k, const double *A, int lda, const do
       const int variant = g_variant.load();
       if (variant == OS2_GEMM_SIMT)
         err = launch_gemm_simt(mi, nj, L.kp, pai, pbj, N, OS2_OUT_MODP_INT8, ci, L.ldcres, t, s);
+      else if (variant == OS2_GEMM_S8_SYNC)
+        err = launch_gemm_s8(mi, nj, L.kp, pai, pbj, N, OS2_OUT_MODP_INT8, ci, L.ldcres, t,
+                             status, s, n);
       else
         err = launch_gemm_tc(variant == OS2_GEMM_TC_1SM ? 0 : (variant == OS2_GEMM_TC_I8 ? 3 : 2), mi, nj, L.kp, pai, pbj, N, ci,
                              L.ldcres, nullptr, nullptr, 14, t, status, s, n);
@@ -1148,8 +1157,9 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
   if (m < 0 || n < 0 || k < 0 || k > ldp || ldp % OS2_KP_ALIGN) return OS2_ERR_INVALID_ARG;
   if (num_moduli < 1 || num_moduli > OS2_MAX_MODULI) return OS2_ERR_INVALID_ARG;
   if (out_kind != OS2_OUT_MODP_INT8 && out_kind != OS2_OUT_RAW_INT32) return OS2_ERR_INVALID_ARG;
-  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM)
-    return OS2_ERR_INVALID_ARG;  // (planes here are FP16; OS2_GEMM_TC_I8 reads int8 ones)
+  if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM &&
+      variant != OS2_GEMM_S8_SYNC)
+    return OS2_ERR_INVALID_ARG;  // (OS2_GEMM_TC_I8 widens int8 planes inside os2_gemm only)
   if (ldo < std::max(n, 1)) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_MODP_INT8 && ldo % OS2_CRES_ALIGN) return OS2_ERR_INVALID_ARG;
   if (out_kind == OS2_OUT_RAW_INT32 && ldo % 4) return OS2_ERR_INVALID_ARG;
@@ -1168,6 +1178,9 @@ os2_status os2_gemm_residues(int m, int n, int k, const void *RA, const void *RB
   if (!t || !status) return OS2_ERR_CUDA;
   if (variant == OS2_GEMM_SIMT)
     return cuda_status(launch_gemm_simt(m, n, ldp, RA, RB, num_moduli, out_kind, out, ldo, t, s));
+  if (variant == OS2_GEMM_S8_SYNC)  // int8 planes
+    return cuda_status(
+        launch_gemm_s8(m, n, ldp, RA, RB, num_moduli, out_kind, out, ldo, t, status, s));
   const int kind = out_kind == OS2_OUT_RAW_INT32 ? 1 : (variant == OS2_GEMM_TC_1SM ? 0 : 2);
   return cuda_status(launch_gemm_tc(kind, m, n, ldp, RA, RB, num_moduli, out, ldo, nullptr, nullptr,
                                     14, t, status, s));
@@ -1239,7 +1252,7 @@ os2_status os2_set_crt_variant(int variant) {
 
 os2_status os2_set_gemm_variant(int variant) {
   if (variant != OS2_GEMM_TC && variant != OS2_GEMM_SIMT && variant != OS2_GEMM_TC_1SM &&
-      variant != OS2_GEMM_TC_I8)
+      variant != OS2_GEMM_TC_I8 && variant != OS2_GEMM_S8_SYNC)
     return OS2_ERR_INVALID_ARG;
   g_variant.store(variant);
   return OS2_OK;

@@ -136,6 +136,13 @@ cudaError_t launch_crt_tc(bool f32, int m, int n, const int8_t *c, int ldcres, c
 cudaError_t launch_gemm_simt(int m, int n, int kp, const void *RA, const void *RB, int N,
                              int out_kind, void *out, int ldo, const Os2Tables *t, cudaStream_t s);
 
+// mma.sync s8 GEMM (the INT8 tensor path outside tcgen05) on int8 planes RA
+// [N][m][kp] and RB [N][b_plane_rows][kp] (b_plane_rows 0: n); out_kind as
+// os2_gemm_residues.
+cudaError_t launch_gemm_s8(int m, int n, int kp, const void *RA, const void *RB, int N,
+                           int out_kind, void *out, int ldo, const Os2Tables *t, int *status,
+                           cudaStream_t s, int b_plane_rows = 0);
+
 // tcgen05 GEMM.  kind: 0 = mod-p int8 output (single SM), 1 = exact int32 (raw
 // output and/or row/col maxima), 2 = mod-p int8 output on SM pairs (2-SM MMA),
 // 3 = as 2 from int8 residue planes (widened to FP16 on chip).  prod_bound_log2: log2 of the largest |a*b| of one term

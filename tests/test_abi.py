@@ -102,12 +102,14 @@ def test_argument_errors_are_synchronous():
     assert gr(4, 4, 4, P, P, 64, 14, 0, P, 8, 0, None) == binding.ERR_INVALID_ARG   # ldo % 16 for int8
     assert gr(4, 4, 4, P, P, 64, 14, 2, P, 16, 0, None) == binding.ERR_INVALID_ARG  # out kind
     assert gr(4, 4, 4, P, P, 64, 14, 0, P, 16, 5, None) == binding.ERR_INVALID_ARG  # variant
+    assert gr(4, 4, 4, P, P, 64, 14, 0, P, 16, binding.GEMM_TC_I8, None) == binding.ERR_INVALID_ARG
     big = 1 << 17
     assert gr(4, 4, big, P, P, big, 14, 1, P, 4, 0, None) == binding.ERR_UNSUPPORTED  # raw int32 k limit
     c = lib.os2_crt
     assert c(4, 4, P, 2, 14, P, P, P, 4, None, None) == binding.ERR_INVALID_ARG     # ldcres < n
-    assert lib.os2_set_gemm_variant(4) == binding.ERR_INVALID_ARG
+    assert lib.os2_set_gemm_variant(5) == binding.ERR_INVALID_ARG
     assert lib.os2_set_gemm_variant(binding.GEMM_TC_I8) == binding.OK
+    assert lib.os2_set_gemm_variant(binding.GEMM_S8_SYNC) == binding.OK
     assert lib.os2_set_gemm_variant(binding.GEMM_TC) == binding.OK
     w = lib.os2_wait_selftest
     assert w(0, None, None) == binding.ERR_INVALID_ARG                 # limit < 1

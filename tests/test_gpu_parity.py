@@ -153,29 +153,37 @@ def _planes_pair(m, n, k, N, seed=0, kind="spread", phi=1.0):
     return A, Bt, e, f, os2.residues(dev(A), dev(e), N), os2.residues(dev(Bt), dev(f), N)
 
 
+def _step3(RA, RB, k, out_kind, variant):
+    """os2_gemm_residues on the FP16 planes, or on int8 copies of them for the
+    variant that reads int8 planes."""
+    if variant == os2.GEMM_S8_SYNC:
+        RA, RB = RA.to(torch.int8), RB.to(torch.int8)
+    return os2.gemm_residues(RA, RB, k, out_kind, variant)
+
+
 def _int_product(RA, RB, k):
     a = RA.float().cpu().numpy().astype(np.int64)[:, :, :k]
     b = RB.float().cpu().numpy().astype(np.int64)[:, :, :k]
     return np.einsum("lik,ljk->lij", a, b)
 
 
-@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_SIMT])
+@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_SIMT, os2.GEMM_S8_SYNC])
 @pytest.mark.parametrize("m,n,k", [(128, 128, 64), (129, 257, 65), (300, 200, 1100), (64, 64, 4097)])
 def test_raw_int32_products_bit_exact(variant, m, n, k):
     N = 3
     A, Bt, e, f, RA, RB = _planes_pair(m, n, k, N)
-    G = os2.gemm_residues(RA, RB, k, os2.OUT_RAW_INT32, variant)
+    G = _step3(RA, RB, k, os2.OUT_RAW_INT32, variant)
     status_ok()
     want = _int_product(RA, RB, k)
     assert np.array_equal(G.cpu().numpy()[:, :, :n].astype(np.int64), want)
 
 
-@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_TC_1SM, os2.GEMM_SIMT])
+@pytest.mark.parametrize("variant", [os2.GEMM_TC, os2.GEMM_TC_1SM, os2.GEMM_SIMT, os2.GEMM_S8_SYNC])
 @pytest.mark.parametrize("m,n,k,N", [(128, 256, 64, 2), (513, 700, 3000, 16), (256, 256, 961, 5), (129, 257, 65, 14), (300, 520, 1000, 16),
                                      (256, 512, 2000, 20), (70, 33, 3000, 9)])
 def test_modp_products_bit_exact(variant, m, n, k, N):
     A, Bt, e, f, RA, RB = _planes_pair(m, n, k, N, seed=m)
-    c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, variant)
+    c = _step3(RA, RB, k, os2.OUT_MODP_INT8, variant)
     status_ok()
     rows = np.arange(m, dtype=np.int32)
     cols = np.arange(n, dtype=np.int32)
@@ -190,11 +198,12 @@ def test_int32_accumulation_worst_case():
     k = (1 << 17) - 64
     RA = torch.full((1, 128, k), -128.0, dtype=torch.float16, device=DEV)
     RB = torch.full((1, 128, k), -128.0, dtype=torch.float16, device=DEV)
-    G = os2.gemm_residues(RA, RB, k, os2.OUT_RAW_INT32, os2.GEMM_TC)
-    status_ok()
-    assert torch.all(G[:, :, :128] == 16384 * k)
-    for variant in (os2.GEMM_TC, os2.GEMM_TC_1SM):
-        c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, variant)
+    for variant in (os2.GEMM_TC, os2.GEMM_S8_SYNC):
+        G = _step3(RA, RB, k, os2.OUT_RAW_INT32, variant)
+        status_ok()
+        assert torch.all(G[:, :, :128] == 16384 * k), variant
+    for variant in (os2.GEMM_TC, os2.GEMM_TC_1SM, os2.GEMM_S8_SYNC):
+        c = _step3(RA, RB, k, os2.OUT_MODP_INT8, variant)
         status_ok()
         assert torch.all(c[:, :, :128] == 0)   # 2^14 k is a multiple of 256
 
@@ -214,8 +223,10 @@ def test_modp_alternating_extremes():
     RA, RB = dev(ra), dev(rb)
     c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC).cpu().numpy()[:, :, :n]
     c1 = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_TC_1SM).cpu().numpy()[:, :, :n]
+    c8 = _step3(RA, RB, k, os2.OUT_MODP_INT8, os2.GEMM_S8_SYNC).cpu().numpy()[:, :, :n]
     status_ok()
     assert np.array_equal(c, c1)
+    assert np.array_equal(c, c8)
     G = np.einsum("lik,ljk->lij", ra.astype(np.int64), rb.astype(np.int64))
     for l, p in enumerate(mods):
         r = np.mod(G[l], p)
@@ -332,7 +343,8 @@ def test_gemm_64cube_normal_config():
     assert_bits_equal(C, ref.C, "64^3")
 
 
-@pytest.mark.parametrize("variant", [os2.GEMM_SIMT, os2.GEMM_TC_1SM, os2.GEMM_TC_I8])
+@pytest.mark.parametrize("variant", [os2.GEMM_SIMT, os2.GEMM_TC_1SM, os2.GEMM_TC_I8,
+                                     os2.GEMM_S8_SYNC])
 def test_gemm_variants_end_to_end(variant):
     A, Bt = workloads.make_pair("spread", 150, 170, 400, seed=1, phi=2.0)
     try:
@@ -347,17 +359,19 @@ def test_gemm_variants_end_to_end(variant):
     assert_bits_equal(Ct, ref.C, "tc vs oracle")
 
 
+@pytest.mark.parametrize("variant", [os2.GEMM_TC_I8, os2.GEMM_S8_SYNC])
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
 @pytest.mark.parametrize("m,n,k,N", [(4100, 300, 700, 16), (257, 513, 1921, 20), (3, 5, 7, 2),
                                      (300, 260, 9000, 14)])
-def test_int8_plane_variant_oracle(mode, m, n, k, N):
-    """The int8-plane variant (step 2 writes int8 residue planes, step 3 widens
-    them to FP16 on chip): bit-exact against the oracle on a sample, with row
-    panels (m >= 4096), ragged tiles, long k (several reduction chunks) and
-    the host entry point's column panels."""
+def test_int8_plane_variant_oracle(variant, mode, m, n, k, N):
+    """The int8-plane variants (step 2 writes int8 residue planes; step 3
+    widens them to FP16 on chip, or multiplies them with mma.sync s8):
+    bit-exact against the oracle on a sample, with row panels (m >= 4096),
+    ragged tiles, long k (several reduction chunks) and the host entry point's
+    column panels."""
     A, Bt = workloads.make_pair("spread", m, n, k, seed=m + k, phi=2.0)
     try:
-        os2.set_gemm_variant(os2.GEMM_TC_I8)
+        os2.set_gemm_variant(variant)
         C = os2.gemm(dev(A), dev(Bt), N, mode).cpu().numpy()
         status_ok()
         Ch = torch.full((m, n), np.nan, dtype=torch.float64).pin_memory()
@@ -569,8 +583,8 @@ def test_modp_products_far_beyond_int32():
     N, m, n, k = 5, 128, 256, 1 << 20
     RA = torch.full((N, m, k), -128.0, dtype=torch.float16, device=DEV)
     RB = torch.full((N, n, k), -128.0, dtype=torch.float16, device=DEV)
-    for variant in (os2.GEMM_TC, os2.GEMM_TC_1SM):
-        c = os2.gemm_residues(RA, RB, k, os2.OUT_MODP_INT8, variant).cpu().numpy()[:, :, :n]
+    for variant in (os2.GEMM_TC, os2.GEMM_TC_1SM, os2.GEMM_S8_SYNC):
+        c = _step3(RA, RB, k, os2.OUT_MODP_INT8, variant).cpu().numpy()[:, :, :n]
         status_ok()
         for l, p in enumerate(os2.moduli(N)):
             r = (16384 * k) % p
