@@ -391,10 +391,11 @@ def run_ours(a):
     # algorithmic work per step; a step with A in row panels launches steps 3-5
     # once per panel, each launch doing its share
     kp = (k + 63) // 64 * 64
+    pb = 1.0 if a.gemm in ("tc_i8", "s8") else 2.0  # bytes per residue in the planes
     algo = {
         "scale": ("GB/s", 8.0 * (m + n) * k),
         "scale_bars": ("GB/s", 8.0 * (m + n) * k + 2.0 * (m + n) * kp),
-        "residues": ("GB/s", 8.0 * (m + n) * k + 2.0 * N * (m + n) * kp),
+        "residues": ("GB/s", 8.0 * (m + n) * k + pb * N * (m + n) * kp),
         "gemm_bound": ("TFLOP/s", 2.0 * m * n * k),
         "gemm_modp": ("TFLOP/s", 2.0 * N * m * n * k),
         "crt_unscale": ("GB/s", 1.0 * N * m * n + 8.0 * m * n + 4.0 * (m + n)),
