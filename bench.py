@@ -14,6 +14,9 @@ N > 1 runs under torchrun: every rank multiplies its own independent pair of
 matrices (no collective on the data path; weak scaling), timing is bracketed
 by barriers and the max over ranks is reported.
 
+The line also carries `int8_tensor_path`: the same product with step 3 on
+the INT8 tensor path (mma.sync s8), its rate against the mma.sync s8 probe.
+
 `--impl reference` times the CPU oracle (the exact reference implementation of
 the method) on the host cores, on a bounded sample of output entries of the
 same workload; only rank 0 runs it.
@@ -59,6 +62,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the N in {14,16,18} x {fast, accurate} sweep of the same workload")
+    ap.add_argument("--no-int8", action="store_true",
+                    help="skip the short run of step 3 on the INT8 tensor path (mma.sync s8) "
+                         "that gives the metric's INT8 tensor-pipe utilisation")
     ap.add_argument("--no-peaks", action="store_true",
                     help="skip the tensor-pipe peak probes (own kernels) before the timed steps")
     ap.add_argument("--crt", default="default", choices=["default", "tc", "simt", "auto"],
@@ -519,6 +525,43 @@ def run_ours(a):
                                 "gpu_result_bit_exact_on_sample": same}
         if not same:
             line["parity_error"] = int(np.count_nonzero(got != ref.C))
+
+    # the metric's INT8 half: the same product with step 3 on the INT8 tensor
+    # path (mma.sync s8 on int8 planes), two timed calls; its step-3 rate
+    # against this run's mma.sync s8 probe, and its result against the default's
+    if not a.no_int8 and a.gemm == "tc":
+        ws8 = os2.alloc_workspace(os2.workspace_size(m, n, k, N, a.mode), dev)
+        C8 = torch.empty((m, n), dtype=torch.float64, device=dev)
+        os2.set_gemm_variant(os2.GEMM_S8_SYNC)
+        try:
+            os2.gemm(Ad, Bd, N, a.mode, out=C8, workspace=ws8, stream=stream)
+            torch.cuda.synchronize(dev)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            os2.profile_start()
+            s0.record(stream)
+            for _ in range(2):
+                os2.gemm(Ad, Bd, N, a.mode, out=C8, workspace=ws8, stream=stream)
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            prof8 = os2.profile_stop()
+        finally:
+            os2.set_gemm_variant(os2.GEMM_TC)
+        if os2.get_status(stream):
+            raise RuntimeError("device status set during the INT8-path run")
+        g8 = prof8.get("gemm_modp")
+        ms8 = g8[0] / g8[1]
+        tops = 2.0 * N * m * n * k / (g8[1] / 2) / (ms8 / 1e3) / 1e12
+        i8 = {"kernel": "k_gemm_s8 (mma.sync.m16n8k32 s8 x s8 -> s32, int8 residue planes)",
+              "step3_ms_per_launch": ms8, "step3_tops": tops,
+              "emulated_tflops": flop / (s0.elapsed_time(s1) / 2 / 1e3) / 1e12,
+              "bit_identical_to_default": bool(torch.equal(C8, Cd))}
+        if peaks_probe:
+            i8["peak_tops"] = peaks_probe["mma_sync_s8"]["best"]
+            i8["frac"] = tops / i8["peak_tops"]
+            i8["peak_source"] = "own mma.sync s8 probe of this run (of measured)"
+        line["int8_tensor_path"] = i8
+        del ws8, C8
+        torch.cuda.empty_cache()
 
     # the rest of the 8192^3 configuration: N in {14, 16, 18}, both modes
     if not a.no_sweep:
