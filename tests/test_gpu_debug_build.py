@@ -2,7 +2,7 @@
 indices against the extent of the array they address, records
 OS2_ERR_BOUNDS on a failure and skips the access.  Built here, loaded in a
 fresh process (OS2_LIB), and run over small parity shapes -- both modes, both
-CRT kernels, row panels, the host entry point, the int8-plane variant, SGEMM
+CRT kernels, row panels, the host entry point, the int8-plane variants, SGEMM
 and the CRT alone: every status must stay clean and every result must equal
 the oracle's bits."""
 import os
@@ -52,6 +52,12 @@ for mode in ("fast", "accurate"):
     check(Ch.numpy(), A, Bt, 16, mode, rows, cols)
 os2.set_gemm_variant(os2.GEMM_TC_I8)
 check(os2.gemm(dev(A), dev(Bt), 16, "fast").cpu().numpy(), A, Bt, 16, "fast", rows, cols)
+os2.set_gemm_variant(os2.GEMM_S8_SYNC)
+check(os2.gemm(dev(A), dev(Bt), 16, "fast").cpu().numpy(), A, Bt, 16, "fast", rows, cols)
+Ch = torch.empty((m, n), dtype=torch.float64).pin_memory()
+os2.gemm_host(torch.from_numpy(A).pin_memory(), torch.from_numpy(Bt).pin_memory(), Ch, 16, "accurate")
+torch.cuda.synchronize()
+check(Ch.numpy(), A, Bt, 16, "accurate", rows, cols)
 os2.set_gemm_variant(os2.GEMM_TC_1SM)
 check(os2.gemm(dev(A), dev(Bt), 16, "accurate").cpu().numpy(), A, Bt, 16, "accurate", rows, cols)
 os2.set_gemm_variant(os2.GEMM_TC)
