@@ -100,6 +100,22 @@ def test_config_8192cube_spread(mode):
         torch.cuda.empty_cache()
 
 
+def test_config_8192cube_int8_tensor_path():
+    """The benchmark's workload (8192^3, 16 moduli, fast) with step 3 on the INT8
+    tensor path (mma.sync s8 on int8 residue planes): 4096 sampled entries
+    against the oracle, and every entry equal to the default path's."""
+    A, Bt = workloads.make_pair("spread", 8192, 8192, 8192, seed=0, phi=0.5)
+    Ad, Bd, C = run(A, Bt, 16, "fast")
+    os2.set_gemm_variant(os2.GEMM_S8_SYNC)
+    try:
+        C8 = os2.gemm(Ad, Bd, 16, "fast")
+        assert os2.get_status() == 0
+    finally:
+        os2.set_gemm_variant(os2.GEMM_TC)
+    assert torch.equal(C8, C)
+    check_sample(A, Bt, C8, 16, "fast", count=64)
+
+
 def test_config_16384sq_k32768_spread():
     """m = n = 16384, k = 32768, (U-0.5) exp(N(0,1)), 18 moduli, fast mode."""
     A, Bt = workloads.make_pair("spread", 16384, 16384, 32768, seed=0, phi=1.0)
