@@ -78,3 +78,53 @@ def test_random_configuration_bit_exact(case):
     assert ref.mismatches == 0
     assert _bits_equal(C, ref.C), f"os2_gemm: {np.count_nonzero(C != ref.C)} entries differ"
     assert _bits_equal(Ch.numpy(), ref.C), "os2_gemm_host differs from the oracle"
+
+
+def _cases_other(count=40, seed=3031):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(count):
+        m, n, k = (int(x) for x in rng.integers(1, 161, 3))
+        what = str(rng.choice(["sgemm", "zgemm", "cgemm"]))
+        N = int(rng.integers(1, 21))
+        mode = "fast" if rng.random() < 0.5 else "accurate"
+        phi = float(rng.choice([0.5, 2.0, 4.0]))
+        variant = VARIANTS[int(rng.integers(len(VARIANTS)))]
+        out.append((i, what, m, n, k, N, mode, phi, variant))
+    return out
+
+
+@pytest.mark.parametrize("case", _cases_other(), ids=lambda c: "c%d_%s_%dx%dx%d_N%d_%s_v%d"
+                         % (c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[8]))
+def test_random_sgemm_complex_bit_exact(case):
+    """The same sweep for the SGEMM and complex products ([G] Ergebnisse and
+    Bedeutung), against the oracle's binary32 rounding and its real block form."""
+    i, what, m, n, k, N, mode, phi, variant = case
+    omode = orc.FAST if mode == "fast" else orc.ACCURATE
+    A, Bt = workloads.make_pair("spread", m, n, k, seed=300 + i, phi=phi)
+    os2.set_gemm_variant(variant)
+    try:
+        if what == "sgemm":
+            A32, B32 = A.astype(np.float32), Bt.astype(np.float32)
+            C = os2.sgemm(torch.from_numpy(A32).cuda(), torch.from_numpy(B32).cuda(), N,
+                          mode).cpu().numpy()
+        else:
+            Ai, Bi = workloads.make_pair("spread", m, n, k, seed=400 + i, phi=phi)
+            dt = np.complex64 if what == "cgemm" else np.complex128
+            Z, W = (A + 1j * Ai).astype(dt), (Bt + 1j * Bi).astype(dt)
+            C = os2.zgemm(torch.from_numpy(Z).cuda(), torch.from_numpy(W).cuda(), N,
+                          mode).cpu().numpy()
+        st = os2.get_status()
+        assert st == 0, os2.status_string(st)
+    finally:
+        os2.set_gemm_variant(os2.GEMM_TC)
+    if what == "sgemm":
+        ref = orc.gemm_entries(A32, B32, N, mode=omode, want_X=False, want_c=False, want_G=False,
+                               out_f32=True)
+        assert ref.mismatches == 0
+        assert np.array_equal(C.view(np.uint32), ref.C.view(np.uint32))
+    else:
+        ref, r = orc.complex_gemm_entries(Z, W, N, mode=omode, single=what == "cgemm")
+        assert r.mismatches == 0
+        view = np.uint32 if what == "cgemm" else np.uint64
+        assert np.array_equal(C.view(view), ref.view(view))
