@@ -362,6 +362,10 @@ def gemm_residues(RA, RB, k, out_kind=OUT_MODP_INT8, variant=GEMM_TC, stream=Non
     Returns int8 [N, m, ldo] (mod p, symmetric) or int32 [N, m, ldo] (raw)."""
     N, m, ldp = RA.shape
     n = RB.shape[1]
+    want = torch.int8 if variant == GEMM_S8_SYNC else torch.float16
+    if RA.dtype != want or RB.dtype != want:
+        raise TypeError(f"gemm_residues: variant {variant} takes {want} planes, got "
+                        f"{RA.dtype} and {RB.dtype}")
     if out_kind == OUT_MODP_INT8:
         ldo = (max(n, 1) + CRES_ALIGN - 1) // CRES_ALIGN * CRES_ALIGN
         out = torch.empty((N, m, ldo), dtype=torch.int8, device=RA.device)

@@ -122,3 +122,15 @@ def test_binding_raises_without_fallback(monkeypatch):
     monkeypatch.setattr(binding._build, "LIB", "/nonexistent/libos2.so")
     with pytest.raises(RuntimeError):
         binding.load(build_if_missing=False)
+
+
+def test_gemm_residues_checks_plane_dtype():
+    """The int8-plane variant takes int8 planes, the others FP16 ones; a
+    mismatch is refused before any call into the library."""
+    import torch
+    f16 = torch.zeros((1, 4, 64), dtype=torch.float16)
+    i8 = torch.zeros((1, 4, 64), dtype=torch.int8)
+    with pytest.raises(TypeError):
+        binding.gemm_residues(f16, f16, 64, variant=binding.GEMM_S8_SYNC)
+    with pytest.raises(TypeError):
+        binding.gemm_residues(i8, i8, 64, variant=binding.GEMM_TC)
