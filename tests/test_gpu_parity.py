@@ -362,12 +362,13 @@ def test_gemm_variants_end_to_end(variant):
 @pytest.mark.parametrize("variant", [os2.GEMM_TC_I8, os2.GEMM_S8_SYNC])
 @pytest.mark.parametrize("mode", ["fast", "accurate"])
 @pytest.mark.parametrize("m,n,k,N", [(4100, 300, 700, 16), (257, 513, 1921, 20), (3, 5, 7, 2),
-                                     (300, 260, 9000, 14)])
+                                     (300, 260, 9000, 14), (64, 48, 70000, 16)])
 def test_int8_plane_variant_oracle(variant, mode, m, n, k, N):
     """The int8-plane variants (step 2 writes int8 residue planes; step 3
     widens them to FP16 on chip, or multiplies them with mma.sync s8):
     bit-exact against the oracle on a sample, with row panels (m >= 4096),
-    ragged tiles, long k (several reduction chunks) and the host entry point's
+    ragged tiles, long k (several reduction chunks; k = 70000 crosses the
+    65536-term reduction of the mma.sync kernel) and the host entry point's
     column panels."""
     A, Bt = workloads.make_pair("spread", m, n, k, seed=m + k, phi=2.0)
     try:
