@@ -31,9 +31,10 @@
  *    native-FP64 accuracy ([Q] "行列積の回数と性能").
  *  - 0 <= k < 2^24.  [Q] "誤差のないINT8行列積(手順3)": INT32 sums of residue
  *    products are exact only while k < 2^17, and larger k is split into
- *    blocks.  Here step 3 reduces every 960-term block mod p_l inside tensor
- *    memory, so that split is built in and the mod-p products have no such
- *    limit.  Remaining limits: accurate mode k < 2^19 (its exact int32 bound
+ *    blocks.  Here step 3 reduces its partial sums mod p_l block by block (at
+ *    most 960 terms per block in tensor memory, 65536 in the mma.sync
+ *    variant's int32 registers), so that split is built in and the mod-p
+ *    products have no such limit.  Remaining limits: accurate mode k < 2^19 (its exact int32 bound
  *    product), raw int32 products from os2_gemm_residues k < 2^17.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Every device-side entry point only enqueues work on it and
