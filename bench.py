@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the N in {14,16,18} x {fast, accurate} sweep of the same workload")
+    ap.add_argument("--e2e-calls", type=int, default=150,
+                    help="timed os2_gemm_host calls of the e2e measurement (about 12 ms each at "
+                         "8192^3; every call counts, stalls included)")
     ap.add_argument("--no-int8", action="store_true",
                     help="skip the short run of step 3 on the INT8 tensor path (mma.sync s8) "
                          "that gives the metric's INT8 tensor-pipe utilisation")
@@ -476,7 +479,7 @@ def run_ours(a):
         for _ in range(3):
             os2.gemm_host(Ah, Bh, Ch, N, a.mode, workspace=wsh, stream=stream)
         torch.cuda.synchronize(dev)
-        ke = max(3, min(a.steps, 60))
+        ke = max(3, a.e2e_calls)
         barrier(world)
         # one event per call as well: the host link is shared with the machine's
         # other tenants, so the spread of single calls is reported beside the mean
